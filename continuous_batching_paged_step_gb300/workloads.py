@@ -1,0 +1,203 @@
+"""Seeded synthetic inputs for one packed continuous-batching step.
+
+This module is the only code shared by the CUDA path (tests, bench) and the
+CPU oracle.  It draws numbers and lays out integer metadata; it holds none of
+the method's arithmetic (no slot mapping, no masking, no attention).
+
+Shapes follow the mixed-batch example of page "11.2 连续批处理与 PagedAttention"
+(section 11.2.2, Figure 11-3): Q rows are [T, n_q*128] and new K/V rows are
+[T, n_kv*128] with head h occupying columns [h*128, (h+1)*128).  bf16 values
+are carried as uint16 bit patterns, drawn as float32 N(0, 1) and rounded to
+nearest-even.
+
+Every array of request r is drawn from its own stream, seeded by
+(step seed, r, stream kind), so any subset of requests can be regenerated
+alone and large steps can be generated on several threads.
+"""
+from __future__ import annotations
+
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import numpy as np
+
+BLOCK_SIZE = 16
+N_Q_HEADS = 32
+N_KV_HEADS = 8
+HEAD_DIM = 128
+
+_KIND_Q, _KIND_KNEW, _KIND_VNEW, _KIND_KPRIOR, _KIND_VPRIOR = range(5)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even); return uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to float32 (exact)."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _normal_bf16(seed: int, r: int, kind: int, shape) -> np.ndarray:
+    rng = np.random.default_rng([seed, r, kind])
+    n = int(np.prod(shape))
+    return f32_to_bf16_bits(rng.standard_normal(n, dtype=np.float32)).reshape(shape)
+
+
+@dataclass
+class StepSpec:
+    """One packed step: request r brings q_lens[r] new rows after ctx_lens[r] cached tokens."""
+    name: str
+    q_lens: list
+    ctx_lens: list
+    num_blocks: int
+    seed: int
+    n_q_heads: int = N_Q_HEADS
+    n_kv_heads: int = N_KV_HEADS
+    head_dim: int = HEAD_DIM
+    block_size: int = BLOCK_SIZE
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def num_reqs(self) -> int:
+        return len(self.q_lens)
+
+    @property
+    def num_tokens(self) -> int:
+        return int(sum(self.q_lens))
+
+    def blocks_needed(self, r: int) -> int:
+        return -(-(self.ctx_lens[r] + self.q_lens[r]) // self.block_size)
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return max(1, max(self.blocks_needed(r) for r in range(self.num_reqs)))
+
+
+@dataclass
+class StepInputs:
+    spec: StepSpec
+    q: np.ndarray              # uint16 [T, n_q*d]
+    k_new: np.ndarray          # uint16 [T, n_kv*d]
+    v_new: np.ndarray          # uint16 [T, n_kv*d]
+    k_prior: list              # per request uint16 [ctx_r, n_kv*d]
+    v_prior: list
+    cu_seqlens_q: np.ndarray   # int32 [R+1]
+    context_lens: np.ndarray   # int32 [R]
+    block_tables: np.ndarray   # int32 [R, max_blocks]; unused entries are -1
+    block_order: np.ndarray    # int32: physical ids in the order they were handed out
+
+
+def _threads() -> int:
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def make_inputs(spec: StepSpec, with_prior: bool = True, requests=None) -> StepInputs:
+    """Draw every array of the step.  `requests` restricts the per-request prior K/V
+    (the packed Q/K/V rows are always complete); other prior entries are None."""
+    R, T = spec.num_reqs, spec.num_tokens
+    hq, hk, d = spec.n_q_heads, spec.n_kv_heads, spec.head_dim
+    cu = np.zeros(R + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(np.asarray(spec.q_lens, dtype=np.int64))
+    ctx = np.asarray(spec.ctx_lens, dtype=np.int32)
+
+    perm = np.random.default_rng([spec.seed, 0x7AB1E]).permutation(spec.num_blocks).astype(np.int32)
+    need = [spec.blocks_needed(r) for r in range(R)]
+    if sum(need) > spec.num_blocks:
+        raise ValueError(f"{spec.name}: {sum(need)} blocks needed, pool has {spec.num_blocks}")
+    tables = np.full((R, spec.max_blocks_per_seq), -1, dtype=np.int32)
+    off = 0
+    for r in range(R):
+        tables[r, :need[r]] = perm[off:off + need[r]]
+        off += need[r]
+
+    def rows(r):
+        ql = spec.q_lens[r]
+        return (_normal_bf16(spec.seed, r, _KIND_Q, (ql, hq * d)),
+                _normal_bf16(spec.seed, r, _KIND_KNEW, (ql, hk * d)),
+                _normal_bf16(spec.seed, r, _KIND_VNEW, (ql, hk * d)))
+
+    want = set(range(R)) if requests is None else set(requests)
+
+    def prior(r):
+        if not with_prior or r not in want:
+            return None, None
+        c = spec.ctx_lens[r]
+        return (_normal_bf16(spec.seed, r, _KIND_KPRIOR, (c, hk * d)),
+                _normal_bf16(spec.seed, r, _KIND_VPRIOR, (c, hk * d)))
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        new_rows = list(ex.map(rows, range(R)))
+        priors = list(ex.map(prior, range(R)))
+
+    def cat(i, width):
+        parts = [nr[i] for nr in new_rows if nr[i].shape[0] > 0]
+        return np.concatenate(parts, axis=0) if parts else np.zeros((0, width), np.uint16)
+
+    return StepInputs(spec=spec, q=cat(0, hq * d), k_new=cat(1, hk * d), v_new=cat(2, hk * d),
+                      k_prior=[p[0] for p in priors], v_prior=[p[1] for p in priors],
+                      cu_seqlens_q=cu, context_lens=ctx, block_tables=tables,
+                      block_order=perm[:off].copy())
+
+
+# --------------------------------------------------------------------------------------
+# The step shapes.  Sizes follow the workloads described for the method: the 3-request
+# mixed step of page "11.2 连续批处理与 PagedAttention" (section 11.2.2), decode rows over
+# long cached histories, and chunked prefill under an 8192-token budget (section 11.2.5).
+# --------------------------------------------------------------------------------------
+
+def tiny_p5_step(seed: int = 0xC0FFEE + 1) -> StepSpec:
+    """R1 prefills 5 tokens with nothing cached; R2 and R3 decode one token after 7 and 3
+    cached tokens; pool of 64 blocks."""
+    return StepSpec("tiny-3req", q_lens=[5, 1, 1], ctx_lens=[0, 7, 3], num_blocks=64, seed=seed)
+
+
+def mixed_step(seed: int = 0xC0FFEE + 2) -> StepSpec:
+    """64 decode rows with context ~ U[128, 4096] plus two 512-token prefill chunks with
+    0 and 1024 tokens cached; pool of 32768 blocks."""
+    rng = np.random.default_rng([seed, 1])
+    dec_ctx = rng.integers(128, 4096, size=64, endpoint=True).tolist()
+    return StepSpec("mixed-64dec-2x512", q_lens=[1] * 64 + [512, 512],
+                    ctx_lens=dec_ctx + [0, 1024], num_blocks=32768, seed=seed)
+
+
+def decode_heavy_step(seed: int = 0xC0FFEE + 3, num_blocks: int = 32768) -> StepSpec:
+    """256 decode rows, context lognormal with median 1024 and sigma 0.8, clipped to [16, 8192]."""
+    rng = np.random.default_rng([seed, 1])
+    ctx = np.clip(np.round(np.exp(math.log(1024.0) + 0.8 * rng.standard_normal(256))), 16, 8192)
+    return StepSpec("decode-256-lognormal", q_lens=[1] * 256, ctx_lens=ctx.astype(int).tolist(),
+                    num_blocks=num_blocks, seed=seed)
+
+
+def chunked_prefill_step(seed: int = 0xC0FFEE + 4, num_blocks: int = 32768) -> StepSpec:
+    """Four 2048-token prefill chunks with 0/2048/4096/6144 cached, plus 32 decode rows
+    with context ~ U[512, 8192] (8224 packed rows)."""
+    rng = np.random.default_rng([seed, 1])
+    dec_ctx = rng.integers(512, 8192, size=32, endpoint=True).tolist()
+    return StepSpec("chunked-4x2048-32dec", q_lens=[2048] * 4 + [1] * 32,
+                    ctx_lens=[0, 2048, 4096, 6144] + dec_ctx, num_blocks=num_blocks, seed=seed)
+
+
+def small_mixed_step(seed: int = 0xC0FFEE + 9, n_decode: int = 12, chunks=((200, 37), (130, 0)),
+                     ctx_range=(1, 700), num_blocks: int = 1024) -> StepSpec:
+    """A small mixed step for the oracle's element-by-element comparison: several decode
+    rows, prefill chunks spanning more than one 128-row tile with a ragged tail, block
+    boundaries crossed at odd offsets."""
+    rng = np.random.default_rng([seed, 1])
+    dec_ctx = rng.integers(ctx_range[0], ctx_range[1], size=n_decode, endpoint=True).tolist()
+    q_lens = [1] * n_decode + [c[0] for c in chunks]
+    ctx = dec_ctx + [c[1] for c in chunks]
+    return StepSpec("small-mixed", q_lens=q_lens, ctx_lens=ctx, num_blocks=num_blocks, seed=seed)
+
+
+CONFIGS = {
+    "tiny": tiny_p5_step,
+    "mixed": mixed_step,
+    "decode": decode_heavy_step,
+    "chunked": chunked_prefill_step,
+}
