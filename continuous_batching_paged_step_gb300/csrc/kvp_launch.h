@@ -1,0 +1,68 @@
+// Host-side interface between the C-ABI layer (kvp_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kvp {
+
+// Scratch layout inside the caller's workspace for one paged_attention_step call.
+// Offsets are in bytes from the workspace base; every region is 256-byte aligned.
+struct StepLayout {
+    int max_decode_items;    // (request, chunk of pages) work items of decode rows
+    int max_partials;        // split-KV partial slots (requests with more than one chunk)
+    int max_prefill_tiles;   // (request, 32-token q tile) work items of prefill chunks
+    int max_combines;        // decode requests whose chunks are merged
+    int decode_chunk_pages;
+    size_t counters_off;     // int32[8]: 0 decode items, 1 prefill tiles, 2 combines
+    size_t decode_items_off; // int4 {r, first_page, n_pages, partial slot or -1}
+    size_t prefill_tiles_off;// int4 {r, first token of tile, tokens in tile, 0}
+    size_t combines_off;     // int4 {r, first slot, n_chunks, 0}
+    size_t part_acc_off;     // float [slot][32 heads][128]  (unnormalised)
+    size_t part_ml_off;      // float2 [slot][32 heads]      (running max (log2 units), sum)
+    size_t total;
+};
+
+StepLayout make_step_layout(int num_reqs, int num_tokens, int max_context_len, int decode_chunk_pages);
+
+struct StepArgs {
+    const void* q;
+    void* out;
+    const int32_t* cu_seqlens_q;
+    const int32_t* context_lens;
+    const int32_t* block_tables;
+    int max_blocks_per_seq;
+    int num_reqs;
+    int num_tokens;
+    int max_q_len;
+    int max_context_len;
+    float softmax_scale;
+    const void* k_cache;
+    const void* v_cache;
+    int num_blocks;
+    uint32_t* err;
+    char* ws;
+    StepLayout lay;
+    int num_sms;
+};
+
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t* cu, const int32_t* ctx,
+                             const int32_t* tables, int max_blocks, int num_reqs, int num_tokens, void* k_cache,
+                             void* v_cache, const int32_t* refcnt, int num_blocks, uint32_t* err,
+                             cudaStream_t stream);
+
+cudaError_t launch_step_prep(const StepArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream);
+cudaError_t launch_combine(const StepArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill(const StepArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
+                           const CUtensorMap* tmap_v, cudaStream_t stream);
+
+// One-time per-device kernel attributes (dynamic shared memory limits).
+cudaError_t configure_kernels();
+
+// Tokens per prefill q tile (x 4 query heads of one KV group = 128 MMA rows).
+constexpr int kPrefillTileTokens = 32;
+
+}  // namespace kvp

@@ -1,0 +1,240 @@
+"""Thin Python binding of libkvpaged.so (the C ABI in include/kvpaged.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA kernels.
+PyTorch supplies device memory and streams.  Importing this module fails loudly when
+the library has not been built; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkvpaged.so")
+
+KVP_OK = 0
+STATUS_NAMES = {0: "KVP_OK", -1: "KVP_E_INVALID_ARG", -2: "KVP_E_NO_BLOCKS", -3: "KVP_E_BAD_BLOCK",
+                -4: "KVP_E_SHARED_WRITE", -5: "KVP_E_BAD_META", -6: "KVP_E_CUDA", -7: "KVP_E_REFCOUNT",
+                -8: "KVP_E_WORKSPACE", -9: "KVP_E_TIMEOUT"}
+ERRBIT_BAD_BLOCK, ERRBIT_SHARED_WRITE, ERRBIT_BAD_META, ERRBIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DTYPE_BF16 = 1
+BLOCK_SIZE, N_KV_HEADS, N_Q_HEADS, HEAD_DIM = 16, 8, 32, 128
+
+# every symbol include/kvpaged.h declares, with (restype, argtypes)
+_P, _I, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+_I32P = ctypes.POINTER(ctypes.c_int32)
+SIGNATURES = {
+    "kv_pool_create": (_I, [_I, _I, _I, _I, _I, _P, _P, ctypes.POINTER(_P)]),
+    "kv_pool_destroy": (_I, [_P]),
+    "kv_block_alloc": (_I, [_P, _I, _I32P]),
+    "kv_block_claim": (_I, [_P, _I, _I32P]),
+    "kv_block_ref": (_I, [_P, _I, _I32P]),
+    "kv_block_free": (_I, [_P, _I, _I32P]),
+    "kv_pool_num_free": (_I, [_P]),
+    "kv_block_refcount": (_I, [_P, ctypes.c_int32]),
+    "kv_append": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "paged_attention_workspace_size": (_SZ, [_P, _I, _I, _I, _I]),
+    "paged_attention_step": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
+    "kv_pool_set_decode_split": (_I, [_P, _I]),
+    "kv_pool_get_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
+    "kvp_status_string": (ctypes.c_char_p, [_I]),
+    "kv_pool_enable_timing": (_I, [_P, _I]),
+    "kv_pool_read_timing": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_F)]),
+    "kv_pool_launch_count": (ctypes.c_longlong, [_P]),
+}
+KERNEL_NAMES = ("kv_append", "step_prep", "prefill_tcgen05", "decode_splitkv", "splitkv_combine")
+
+
+class KVPError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def _check(status: int, what: str):
+    if status != KVP_OK:
+        raise KVPError(status, what)
+
+
+def _ids(ids):
+    a = np.ascontiguousarray(np.asarray(ids, dtype=np.int32).reshape(-1))
+    return a, a.ctypes.data_as(_I32P)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t, dtype, what):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous CUDA tensor of {dtype}")
+
+
+# ------------------------------------------------------------------------ pool
+
+def kv_pool_create(k_cache, v_cache, num_blocks: int | None = None) -> int:
+    """Wrap caller-owned pools bf16 [num_blocks, 8, 16, 128]; returns the pool handle.
+    k_cache/v_cache may be raw device addresses (int) when num_blocks is given."""
+    if isinstance(k_cache, int):
+        nb = int(num_blocks)
+    else:
+        import torch
+        _need(k_cache, torch.bfloat16, "k_cache")
+        _need(v_cache, torch.bfloat16, "v_cache")
+        if tuple(k_cache.shape[1:]) != (N_KV_HEADS, BLOCK_SIZE, HEAD_DIM) or k_cache.shape != v_cache.shape:
+            raise ValueError("pools must be [num_blocks, 8, 16, 128]")
+        nb = k_cache.shape[0]
+    h = _P()
+    _check(lib.kv_pool_create(nb, BLOCK_SIZE, N_KV_HEADS, HEAD_DIM, DTYPE_BF16, _ptr(k_cache), _ptr(v_cache),
+                              ctypes.byref(h)), "kv_pool_create")
+    return h.value
+
+
+def kv_pool_destroy(pool: int):
+    _check(lib.kv_pool_destroy(pool), "kv_pool_destroy")
+
+
+def kv_block_alloc(pool: int, n: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.int32)
+    _check(lib.kv_block_alloc(pool, n, out.ctypes.data_as(_I32P)), "kv_block_alloc")
+    return out
+
+
+def kv_block_claim(pool: int, ids):
+    a, p = _ids(ids)
+    _check(lib.kv_block_claim(pool, a.size, p), "kv_block_claim")
+
+
+def kv_block_ref(pool: int, ids):
+    a, p = _ids(ids)
+    _check(lib.kv_block_ref(pool, a.size, p), "kv_block_ref")
+
+
+def kv_block_free(pool: int, ids):
+    a, p = _ids(ids)
+    _check(lib.kv_block_free(pool, a.size, p), "kv_block_free")
+
+
+def kv_pool_num_free(pool: int) -> int:
+    return lib.kv_pool_num_free(pool)
+
+
+def kv_block_refcount(pool: int, block_id: int) -> int:
+    return lib.kv_block_refcount(pool, block_id)
+
+
+def kv_pool_set_decode_split(pool: int, pages: int):
+    _check(lib.kv_pool_set_decode_split(pool, pages), "kv_pool_set_decode_split")
+
+
+def kv_pool_get_error(pool: int, stream=None):
+    """Synchronise the stream, read and clear the device error word: (status, bits)."""
+    bits = ctypes.c_uint32(0)
+    st = lib.kv_pool_get_error(pool, _stream(stream), ctypes.byref(bits))
+    return st, bits.value
+
+
+def kv_pool_enable_timing(pool: int, max_launches: int):
+    _check(lib.kv_pool_enable_timing(pool, max_launches), "kv_pool_enable_timing")
+
+
+def kv_pool_read_timing(pool: int):
+    """{kernel name: (timed launches, summed ms)} since the last read."""
+    counts = (_I * len(KERNEL_NAMES))()
+    ms = (_F * len(KERNEL_NAMES))()
+    _check(lib.kv_pool_read_timing(pool, counts, ms), "kv_pool_read_timing")
+    return {n: (counts[i], ms[i]) for i, n in enumerate(KERNEL_NAMES)}
+
+
+def kv_pool_launch_count(pool: int) -> int:
+    return lib.kv_pool_launch_count(pool)
+
+
+# ------------------------------------------------------------------ the step
+
+def kv_append(pool: int, k_new, v_new, cu_seqlens_q, context_lens, block_tables, stream=None):
+    """Append this step's K/V rows (bf16 [T, 1024]) into the pool."""
+    import torch
+    T = k_new.shape[0]
+    if T:
+        _need(k_new, torch.bfloat16, "k_new")
+        _need(v_new, torch.bfloat16, "v_new")
+        for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (context_lens, "context_lens"), (block_tables, "block_tables")):
+            _need(t, torch.int32, n)
+    R = context_lens.shape[0]
+    _check(lib.kv_append(pool, _ptr(k_new), _ptr(v_new), _ptr(cu_seqlens_q), _ptr(context_lens),
+                         _ptr(block_tables), block_tables.shape[1], R, T, _stream(stream)), "kv_append")
+
+
+def paged_attention_workspace_size(pool: int, num_reqs: int, num_tokens: int, max_context_len: int) -> int:
+    return lib.paged_attention_workspace_size(pool, num_reqs, num_tokens, N_Q_HEADS, max_context_len)
+
+
+def paged_attention_step(pool: int, q, out, cu_seqlens_q, context_lens, block_tables, max_q_len: int,
+                         max_context_len: int, softmax_scale: float, workspace, stream=None):
+    """Varlen paged attention of the packed rows q (bf16 [T, 4096]) into out (same shape)."""
+    import torch
+    T = q.shape[0]
+    if T:
+        _need(q, torch.bfloat16, "q")
+        _need(out, torch.bfloat16, "out")
+        _need(workspace, torch.uint8, "workspace")
+        for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (context_lens, "context_lens"), (block_tables, "block_tables")):
+            _need(t, torch.int32, n)
+    R = context_lens.shape[0]
+    _check(lib.paged_attention_step(pool, _ptr(q), _ptr(out), _ptr(cu_seqlens_q), _ptr(context_lens),
+                                    _ptr(block_tables), block_tables.shape[1], R, T, N_Q_HEADS, max_q_len,
+                                    max_context_len, float(softmax_scale), _ptr(workspace),
+                                    workspace.numel() if workspace is not None else 0, _stream(stream)),
+           "paged_attention_step")
+
+
+class KVPool:
+    """Owns a pair of device pools and the library handle for them."""
+
+    def __init__(self, num_blocks: int, device="cuda"):
+        import torch
+        shape = (num_blocks, N_KV_HEADS, BLOCK_SIZE, HEAD_DIM)
+        self.k_cache = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        self.v_cache = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        self.num_blocks = num_blocks
+        self.handle = kv_pool_create(self.k_cache, self.v_cache)
+
+    def close(self):
+        if self.handle:
+            kv_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

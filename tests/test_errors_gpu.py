@@ -1,0 +1,114 @@
+"""Device-detected errors: the kernels set bits in the pool's error word, skip the
+offending write or request, and still produce every other output.  No test faults,
+traps or hangs the GPU: every bad input here is one the kernels check for."""
+import numpy as np
+import pytest
+
+import oracle
+from continuous_batching_paged_step_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mods():
+    from continuous_batching_paged_step_gb300 import build
+    build.build()
+    from continuous_batching_paged_step_gb300 import kvpaged, runner
+    return kvpaged, runner
+
+
+def _small():
+    return wl.StepSpec("err", q_lens=[1, 1, 20], ctx_lens=[40, 17, 16], num_blocks=32, seed=31)
+
+
+def test_write_into_shared_block_is_refused(mods):
+    kp, runner = mods
+    inp = wl.make_inputs(_small())
+    step = runner.PagedStep(inp)
+    try:
+        # request 0 (40 cached + 1 new) writes position 40 into its third block; share it
+        b = int(inp.block_tables[0, 40 // 16])
+        kp.kv_block_ref(step.pool.handle, [b])
+        before = step.pool.k_cache[b].clone()
+        step.append()
+        st, bits = step.error()
+        assert st == -4
+        assert bits & kp.ERRBIT_SHARED_WRITE
+        assert step.pool.k_cache[b].equal(before)         # the write was skipped
+        # once the share is dropped the same append goes through
+        kp.kv_block_free(step.pool.handle, [b])
+        step.append()
+        assert step.error() == (0, 0)
+    finally:
+        step.close()
+
+
+def test_bad_block_id_is_flagged_and_others_survive(mods):
+    kp, runner = mods
+    import torch
+    inp = wl.make_inputs(_small())
+    step = runner.PagedStep(inp)
+    try:
+        step.run()
+        good = step.out_f32()
+        assert step.error() == (0, 0)
+        # corrupt one entry of request 1's table (a page it reads, not one it writes)
+        step.block_tables[1, 0] = 10 ** 6
+        step.out.zero_()
+        step.attend()
+        st, bits = step.error()
+        assert bits & kp.ERRBIT_BAD_BLOCK
+        got = step.out_f32()
+        cu = inp.cu_seqlens_q
+        for r in (0, 2):
+            s, e = cu[r], cu[r + 1]
+            assert np.array_equal(got[s:e], good[s:e])
+        step.block_tables[1, 0] = int(inp.block_tables[1, 0])
+    finally:
+        step.close()
+
+
+def test_inconsistent_metadata_is_flagged(mods):
+    kp, runner = mods
+    import torch
+    inp = wl.make_inputs(_small())
+    step = runner.PagedStep(inp)
+    try:
+        # cu_seqlens_q that does not end at num_tokens: no work at all, BAD_META
+        bad_cu = step.cu_seqlens_q.clone()
+        bad_cu[-1] += 1
+        kp.paged_attention_step(step.pool.handle, step.q, step.out, bad_cu, step.context_lens, step.block_tables,
+                                step.max_q_len, step.max_context_len, step.softmax_scale, step.workspace)
+        assert step.error()[1] & kp.ERRBIT_BAD_META
+        # a context length above the declared maximum: that request is skipped
+        kp.paged_attention_step(step.pool.handle, step.q, step.out, step.cu_seqlens_q, step.context_lens,
+                                step.block_tables, step.max_q_len, 20, step.softmax_scale, step.workspace)
+        assert step.error()[1] & kp.ERRBIT_BAD_META
+        # a row whose position falls past the table width: kv_append flags and skips it
+        narrow = step.block_tables[:, :2].contiguous()
+        kp.kv_append(step.pool.handle, step.k_new, step.v_new, step.cu_seqlens_q, step.context_lens, narrow)
+        assert step.error()[1] & kp.ERRBIT_BAD_META
+    finally:
+        step.close()
+
+
+def test_host_argument_errors(mods):
+    kp, runner = mods
+    import torch
+    inp = wl.make_inputs(_small())
+    step = runner.PagedStep(inp)
+    try:
+        tiny_ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+        with pytest.raises(kp.KVPError) as e:
+            kp.paged_attention_step(step.pool.handle, step.q, step.out, step.cu_seqlens_q, step.context_lens,
+                                    step.block_tables, step.max_q_len, step.max_context_len, step.softmax_scale,
+                                    tiny_ws)
+        assert e.value.status == -8
+        with pytest.raises(kp.KVPError) as e:
+            kp.paged_attention_step(step.pool.handle, step.q, step.out, step.cu_seqlens_q, step.context_lens,
+                                    step.block_tables, step.max_q_len, step.max_context_len, -1.0, step.workspace)
+        assert e.value.status == -1
+        assert step.error() == (0, 0)      # nothing was launched
+    finally:
+        step.close()

@@ -1,0 +1,174 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+kv_append and block-table indexing must be bit-exact; attention outputs (bf16) must be
+within max-abs 2e-2 and mean-abs 2e-3 of the oracle.  Pools are pre-filled with a NaN
+bit pattern, so a kernel that reads a slot it must not read shows up as NaN.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from continuous_batching_paged_step_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS = 2e-2, 2e-3
+NAN_BITS = 0x7FC1          # a bf16 quiet NaN used to fill pools before a test
+
+
+@pytest.fixture(scope="module")
+def runner():
+    from continuous_batching_paged_step_gb300 import build
+    build.build()
+    from continuous_batching_paged_step_gb300 import runner as r
+    return r
+
+
+def _compare(got, want, rows=None, what=""):
+    if rows is not None:
+        got, want = got[rows], want[rows]
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got.astype(np.float64) - want)
+    worst = np.unravel_index(np.argmax(err), err.shape)
+    assert err.max() <= MAX_ABS, f"{what}: max-abs {err.max():.3e} at {worst}"
+    assert err.mean() <= MEAN_ABS, f"{what}: mean-abs {err.mean():.3e}"
+    return err.max(), err.mean()
+
+
+def _oracle_pool(inp, fill_bits):
+    spec = inp.spec
+    shape = (spec.num_blocks, spec.n_kv_heads, spec.block_size, spec.head_dim)
+    kc = np.full(shape, fill_bits, np.uint16)
+    vc = np.full(shape, fill_bits, np.uint16)
+    ctx = inp.context_lens
+    cu0 = np.concatenate([[0], np.cumsum(ctx)]).astype(np.int32)
+    kp_ = [k for k in inp.k_prior if k is not None and k.shape[0]]
+    vp_ = [v for v in inp.v_prior if v is not None and v.shape[0]]
+    if kp_:
+        kc, vc = oracle.reference_cache_write(kc, vc, np.concatenate(kp_), np.concatenate(vp_), cu0,
+                                              np.zeros_like(ctx), inp.block_tables, spec.n_kv_heads, spec.head_dim)
+    return oracle.reference_cache_write(kc, vc, inp.k_new, inp.v_new, inp.cu_seqlens_q, inp.context_lens,
+                                        inp.block_tables, spec.n_kv_heads, spec.head_dim)
+
+
+def _pool_bits(step):
+    k = step.pool.k_cache.view(__import__("torch").int16).cpu().numpy().view(np.uint16)
+    v = step.pool.v_cache.view(__import__("torch").int16).cpu().numpy().view(np.uint16)
+    return k, v
+
+
+def _run_full_check(runner, spec, split=None):
+    inp = wl.make_inputs(spec)
+    step = runner.PagedStep(inp, pool_fill_bits=NAN_BITS, decode_split_pages=split)
+    try:
+        step.run()
+        st, bits = step.error()
+        assert (st, bits) == (0, 0)
+        k, v = _pool_bits(step)
+        ok_k, ok_v = _oracle_pool(inp, NAN_BITS)
+        assert np.array_equal(k, ok_k) and np.array_equal(v, ok_v), "pool differs from the oracle's cache write"
+        return _compare(step.out_f32(), oracle.step_reference(inp), what=spec.name)
+    finally:
+        step.close()
+
+
+def test_three_request_example(runner):
+    # page "11.2 连续批处理与 PagedAttention", section 11.2.2: R1 prefill 5 (nothing cached),
+    # R2 decode with 7 cached, R3 decode with 3 cached; 64-block pool
+    _run_full_check(runner, wl.tiny_p5_step())
+
+
+def test_small_mixed_step_all_rows(runner):
+    # prefill chunks spanning several 32-token q tiles with ragged tails, one of them after
+    # a cached prefix that ends mid-block; decode rows with varied contexts
+    _run_full_check(runner, wl.small_mixed_step())
+
+
+@pytest.mark.parametrize("split", [1, 3, 32])
+def test_decode_split_and_combine(runner, split):
+    spec = wl.small_mixed_step(seed=77, n_decode=20, chunks=(), ctx_range=(0, 1500), num_blocks=4096)
+    _run_full_check(runner, spec, split=split)
+
+
+def test_edge_cases(runner):
+    # an empty request in the middle, decode at positions 0 / 15 / 16 / 31 / 32 / 8192,
+    # prefill of 2 rows, a 33-row chunk (two q tiles, one row in the second), a chunk whose
+    # cached prefix ends exactly on a 128-key tile boundary and one just before it
+    q_lens = [1, 1, 0, 1, 1, 1, 1, 2, 33, 40, 17]
+    ctx = [0, 15, 9, 16, 31, 32, 8192, 0, 5, 128, 127]
+    spec = wl.StepSpec("edges", q_lens=q_lens, ctx_lens=ctx, num_blocks=1200, seed=4242)
+    _run_full_check(runner, spec)
+
+
+def test_chunked_prefill_matches_one_shot(runner):
+    # The same 300-token prompt run as chunks of 100, 150 and 50 over three steps through
+    # the pool equals one-shot causal prefill (chunked prefill, page "Continuous Batching
+    # 深入实现", section "第三层：Chunked Prefill").
+    import torch
+    from continuous_batching_paged_step_gb300 import kvpaged as kp
+    full = wl.StepSpec("prompt300", q_lens=[300], ctx_lens=[0], num_blocks=64, seed=99)
+    inp = wl.make_inputs(full)
+    want = oracle.step_reference(inp)
+    step = runner.PagedStep(inp, pool_fill_bits=NAN_BITS)
+    try:
+        done = 0
+        for C in (100, 150, 50):
+            rows = slice(done, done + C)
+            dev = step.device
+            q = step.q[rows].contiguous()
+            out = torch.zeros_like(q)
+            cu = torch.tensor([0, C], dtype=torch.int32, device=dev)
+            ctx = torch.tensor([done], dtype=torch.int32, device=dev)
+            kp.kv_append(step.pool.handle, step.k_new[rows].contiguous(), step.v_new[rows].contiguous(), cu, ctx,
+                         step.block_tables)
+            ws = torch.empty(kp.paged_attention_workspace_size(step.pool.handle, 1, C, done), dtype=torch.uint8,
+                             device=dev)
+            kp.paged_attention_step(step.pool.handle, q, out, cu, ctx, step.block_tables, C, done,
+                                    step.softmax_scale, ws)
+            got = out.float().cpu().numpy().reshape(C, 32, 128)
+            _compare(got, want[rows], what=f"chunk at {done}")
+            done += C
+        assert step.error() == (0, 0)
+    finally:
+        step.close()
+
+
+def _sample_rows(spec, rng, per_req=3):
+    cu = np.concatenate([[0], np.cumsum(spec.q_lens)])
+    rows = []
+    for r, ql in enumerate(spec.q_lens):
+        if ql == 0:
+            continue
+        if ql == 1:
+            rows.append(cu[r])
+        else:
+            pick = {0, ql - 1, 31, 32, ql // 2} | set(rng.integers(0, ql, size=per_req).tolist())
+            rows += [cu[r] + j for j in sorted(pick) if j < ql]
+    return np.array(sorted(set(int(x) for x in rows)))
+
+
+@pytest.mark.parametrize("name", ["mixed", "decode", "chunked"])
+def test_full_size_configs_sampled(runner, name):
+    spec = wl.CONFIGS[name]()
+    inp = wl.make_inputs(spec)
+    step = runner.PagedStep(inp)
+    try:
+        step.run()
+        assert step.error() == (0, 0)
+        rng = np.random.default_rng(5)
+        rows = _sample_rows(spec, rng)
+        if name == "decode":
+            rows = rows[rng.permutation(len(rows))[:48]]
+        want = oracle.step_reference(inp, rows=rows)
+        _compare(step.out_f32(), want, rows=rows, what=name)
+        # kv_append bit-exact at the sampled rows: read each row back through the table
+        k, v = _pool_bits(step)
+        cu = inp.cu_seqlens_q
+        for i in rows[:64]:
+            r = int(np.searchsorted(cu, i, side="right") - 1)
+            p = int(inp.context_lens[r] + i - cu[r])
+            b, off, _ = oracle.physical_slot(inp.block_tables[r], p)
+            assert np.array_equal(k[b, :, off, :].reshape(-1), inp.k_new[i])
+            assert np.array_equal(v[b, :, off, :].reshape(-1), inp.v_new[i])
+    finally:
+        step.close()
