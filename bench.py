@@ -1,0 +1,424 @@
+#!/usr/bin/env python
+"""Benchmark of the continuous-batching paged step on GB300.
+
+One step = one pass of the hot path over one packed batch: kv_append of the step's new
+K/V rows into the 16-token block pool, then paged_attention_step (metadata prep,
+tcgen05 prefill tiles, split-KV decode, combine), all through the C ABI.
+
+Metric: packed query tokens/s per attention layer (T / step time), and the decode
+kernel's KV-read GB/s against the measured HBM peak.  Default workload: the mixed
+step (64 decode rows with context ~ U[128, 4096] plus two 512-token prefill chunks with
+0 and 1024 tokens cached, GQA 32/8, d 128, bf16, 32768-block pool).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config mixed|decode|chunked|tiny]
+  python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+Under torchrun (N > 1) every rank runs its own replica of the step on its own GPU (the
+requests of different replicas are independent: weak scaling, no collective on the
+data path); rank 0 prints one JSON line with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+# The CPU oracle legs run on one core: keep BLAS single-threaded (set before numpy loads).
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+
+METRIC = "packed query tokens/s per attention layer; decode KV-read GB/s vs GB300 HBM peak"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+L2_FLUSH_BYTES = 256 << 20
+CSRC = os.path.join(ROOT, "continuous_batching_paged_step_gb300", "csrc")
+KERNEL_SOURCES = {"decode_splitkv": "attn_decode.cu", "prefill_tcgen05": "attn_prefill.cu",
+                  "kv_append": "kv_append.cu", "step_prep": "attn_prep.cu", "splitkv_combine": "attn_decode.cu"}
+
+
+# ------------------------------------------------------------------ workload algebra
+
+def work_of(spec):
+    """Algorithmic work of one step (what the method must touch, not what a kernel does)."""
+    dec_bytes = 0
+    pairs = 0
+    for q, c in zip(spec.q_lens, spec.ctx_lens):
+        if q == 1:
+            n = c + 1
+            # K+V of every visible key (8 heads x 128 x bf16 x 2), Q and O rows, table entries
+            dec_bytes += n * 4096 + 8192 + 8192 + 4 * (-(-n // 16))
+        elif q > 1:
+            pairs += q * c + q * (q + 1) // 2       # visible (query, key) pairs
+    T = spec.num_tokens
+    return {
+        "decode_bytes": dec_bytes,
+        # QK^T and P.V over visible pairs: 2 x 2 x 128 FLOPs per pair per query head
+        "prefill_flops": pairs * 32 * 2 * 2 * 128,
+        # kv_append reads T new K/V rows and writes them into the pool
+        "append_bytes": T * 2048 * 2 * 2,
+    }
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), \
+            "measured (MEASURED_PEAKS.json)"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def source_sha(kernel):
+    with open(os.path.join(CSRC, KERNEL_SOURCES[kernel]), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on this source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = source_sha(kernel)
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+            if kv.get("kernel") == kernel and kv.get("workload") == workload and kv.get("src_sha") == sha:
+                return float(kv["bytes_per_launch"])
+    return None
+
+
+# ------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[6 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[4]) for r in rows if r[4].replace(".", "").isdigit())
+                if any(r[4].replace(".", "").isdigit() for r in rows) else None}
+
+
+# --------------------------------------------------------------------- oracle leg
+
+def oracle_sample_rows(spec, rows_per_chunk):
+    """Every decode row plus `rows_per_chunk` evenly spaced rows of each prefill chunk."""
+    cu = np.concatenate([[0], np.cumsum(spec.q_lens)]).astype(int)
+    rows = []
+    for r, q in enumerate(spec.q_lens):
+        if q == 1:
+            rows.append(int(cu[r]))
+        elif q > 1:
+            k = min(q, rows_per_chunk)
+            rows += sorted(set(int(cu[r] + j) for j in np.linspace(0, q - 1, k).round().astype(int)))
+    return np.array(rows, dtype=np.int64)
+
+
+_ORACLE_INPUTS = {}
+
+
+def time_oracle(config, rows_per_chunk):
+    """Wall time of the oracle (one process, BLAS limited to one thread at start-up) over
+    a sample of the step's rows.  Input generation is outside the timed call."""
+    import oracle
+    from continuous_batching_paged_step_gb300 import workloads as wl
+    if config not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS[config] = wl.make_inputs(wl.CONFIGS[config]())
+    inp = _ORACLE_INPUTS[config]
+    rows = oracle_sample_rows(inp.spec, rows_per_chunk)
+    t0 = time.perf_counter()
+    out = oracle.step_reference(inp, rows=rows)
+    wall = time.perf_counter() - t0
+    assert np.isfinite(out[rows]).all()
+    return len(rows), wall
+
+
+# ---------------------------------------------------------------------- GPU arm
+
+def run_gpu(a):
+    import torch
+    from continuous_batching_paged_step_gb300 import build as b
+    b.build()
+    from continuous_batching_paged_step_gb300 import kvpaged as kp
+    from continuous_batching_paged_step_gb300 import runner, workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    spec = wl.CONFIGS[a.config]()
+    inp = wl.make_inputs(spec)
+    step = runner.PagedStep(inp, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    T = spec.num_tokens
+    work = work_of(spec)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # warm-up
+    for i in range(a.warmup):
+        flush.fill_(i & 0xFF)
+        step.run()
+    torch.cuda.synchronize(dev)
+    st = step.error()
+    if st != (0, 0):
+        raise RuntimeError(f"device error word after warm-up: {st}")
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.25)
+    kp.kv_pool_enable_timing(step.pool.handle, 8 * a.steps + 16)
+    launches0 = kp.kv_pool_launch_count(step.pool.handle)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(a.steps):
+        flush.fill_((i + 1) & 0xFF)        # L2 flush between steps, outside the step's events
+        starts[i].record(stream)
+        step.run()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    wall = time.perf_counter() - wall0
+    launches = kp.kv_pool_launch_count(step.pool.handle) - launches0
+    per_kernel = kp.kv_pool_read_timing(step.pool.handle)
+    kp.kv_pool_enable_timing(step.pool.handle, 0)
+    clk = clocks.stop()
+    st = step.error()
+    if st != (0, 0):
+        raise RuntimeError(f"device error word after the timed steps: {st}")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * T * a.steps / (total_ms / 1e3)
+
+    # ----------------------------------------------------------- end to end (host buffers)
+    e2e = run_e2e(a, step, stream, dev, flush, dist, world)
+
+    if rank != 0:
+        step.close()
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    kern = {}
+    for name, (n, ms) in per_kernel.items():
+        if n:
+            kern[name] = {"launches": n, "avg_us": 1e3 * ms / n}
+    dec_us = kern.get("decode_splitkv", {}).get("avg_us")
+    pre_us = kern.get("prefill_tcgen05", {}).get("avg_us")
+    dominant = max(kern, key=lambda k: kern[k]["avg_us"] * kern[k]["launches"]) if kern else None
+    rl_decode = None
+    if dec_us:
+        ach = work["decode_bytes"] / (dec_us * 1e-6) / 1e9
+        rl_decode = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(ach / hbm, 4), "traffic": ncu_traffic("decode_splitkv", spec.name),
+                     "kernel": "decode_splitkv", "algorithmic_bytes_per_launch": work["decode_bytes"],
+                     "peak_source": f"hbm_gbs, {peak_src}"}
+    rl_prefill = None
+    if pre_us and work["prefill_flops"]:
+        ach = work["prefill_flops"] / (pre_us * 1e-6) / 1e12
+        rl_prefill = {"bound": "tensor", "achieved": round(ach, 1), "peak": bf16, "unit": "TFLOP/s",
+                      "frac": round(ach / bf16, 4), "traffic": ncu_traffic("prefill_tcgen05", spec.name),
+                      "kernel": "prefill_tcgen05", "algorithmic_flops_per_launch": work["prefill_flops"],
+                      "peak_source": f"bf16_tflops (burst), {peak_src}"}
+    roofline = rl_prefill if dominant == "prefill_tcgen05" else rl_decode
+    secondary = rl_decode if roofline is rl_prefill else rl_prefill
+
+    cpu = None
+    if not a.no_cpu_baseline:
+        n_rows, owall = time_oracle(a.config, a.oracle_rows_per_chunk)
+        cpu = {"value": round(n_rows / owall, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n_rows} of {T} packed rows of the {spec.name} step (every decode row, "
+                         f"{a.oracle_rows_per_chunk} evenly spaced rows per prefill chunk), fp64 numpy, "
+                         f"one process, {owall:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": round(total_ms / a.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": spec.name, "num_tokens": T, "num_reqs": spec.num_reqs,
+                   "decode_rows": sum(1 for q in spec.q_lens if q == 1),
+                   "prefill_chunks": [[q, c] for q, c in zip(spec.q_lens, spec.ctx_lens) if q > 1],
+                   "heads": "32 q / 8 kv, d 128", "block_size": 16, "kv_pool_blocks": spec.num_blocks,
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write outside the step events)",
+                   "parallelism": f"replicas x{world}"},
+        "decode_kv_gbs": rl_decode["achieved"] if rl_decode else None,
+        "roofline": roofline, "roofline_secondary": secondary,
+        "kernels_us": {k: round(v["avg_us"], 2) for k, v in kern.items()},
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": int(launches),
+        "wall_s_timed": round(wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+    step.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+def run_e2e(a, step, stream, dev, flush, dist, world):
+    """Same metric through the C ABI with host buffers: H2D of the step's inputs from pinned
+    memory, the step, D2H of the output, all inside the events."""
+    import torch
+    inp = step.inp
+    names = ("q", "k_new", "v_new", "cu_seqlens_q", "context_lens", "block_tables")
+    host = {n: getattr(step, n).cpu().pin_memory() for n in names}
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    n = max(3, a.steps // 4)
+
+    def one():
+        for nm in names:
+            getattr(step, nm).copy_(host[nm], non_blocking=True)
+        step.run()
+        out_h.copy_(step.out, non_blocking=True)
+
+    for i in range(3):
+        one()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        one()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    total = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if dist is not None:
+        t = torch.tensor([total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total = float(t.item())
+    T = inp.spec.num_tokens
+    return {"value": round(world * T * n / (total / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(a):
+    """The CPU oracle as it stands, on the same workload: each step is the oracle over a
+    bounded sample of the step's rows, sized so the whole run takes a few minutes."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return None
+    from continuous_batching_paged_step_gb300 import workloads as wl
+    spec = wl.CONFIGS[a.config]()
+    workers = 1
+    budget_s = 150.0
+    # first timed probe with a small sample, then size the per-step sample to the budget
+    rows_per_chunk = 4
+    n_rows, w = time_oracle(a.config, rows_per_chunk)
+    per_step_target = budget_s / max(1, a.steps + a.warmup)
+    if w < per_step_target / 2:
+        rows_per_chunk = int(min(max(spec.q_lens), rows_per_chunk * per_step_target / max(w, 1e-3)))
+    times = []
+    for i in range(a.warmup + a.steps):
+        n_rows, w = time_oracle(a.config, rows_per_chunk)
+        if i >= a.warmup:
+            times.append(w)
+    per = statistics.median(times)
+    value = n_rows / per
+    sample = (f"{n_rows} of {spec.num_tokens} packed rows per step of the {spec.name} step (every decode row, "
+              f"{rows_per_chunk} evenly spaced rows per prefill chunk)")
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(per * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": spec.name, "num_tokens": spec.num_tokens, "num_reqs": spec.num_reqs},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": workers, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def main():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", choices=["mixed", "decode", "chunked", "tiny"], default="mixed")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--oracle-rows-per-chunk", type=int, default=256)
+    a = p.parse_args()
+    if a.warmup < 3:
+        p.error("--warmup must be at least 3")
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_gpu(a)
+
+
+if __name__ == "__main__":
+    main()
