@@ -6,25 +6,28 @@
 // Decode streams the whole KV history every step (same page, section "为什么 decode 是
 // bandwidth-bound"), so the kernel is built to keep HBM busy:
 //
-// * Work item = (request, chunk of up to `chunk_pages` 16-token blocks).  One block of
-//   all 8 KV heads is 32 KiB contiguous in the pool, so each block of K and of V arrives
-//   with ONE bulk copy (cp.async.bulk, mbarrier completion) into a 3-stage shared-memory
-//   ring: 64 KiB per stage, 192 KiB in flight per SM.  A dedicated producer warp runs
-//   ahead across pages and items; the kernel is persistent (one CTA per SM, items taken
-//   round-robin).
-// * GQA packing: the 4 query heads of a KV head share every K/V byte read.  Two consumer
-//   warps per KV head (16 warps) split each block's 16 tokens 8/8 and keep separate
-//   online-softmax states, merged at the end of the item.
-// * Scores: a lane holds 16 of the 128 dims of one token (8 lanes per token, 4 tokens per
-//   pass) for all 4 query heads; a 3-step transpose-reduce over the 8 lanes (4 shuffles)
-//   leaves one finished score per lane.  Online softmax in base 2 (scores pre-scaled by
-//   softmax_scale * log2 e) with running max m and sum l per head.
-// * P.V: a lane owns 4 output dims of all 4 heads; weights come from a per-warp
-//   shared-memory slot (broadcast reads); fp32 accumulation.
-// * A request with one chunk writes its bf16 output directly; otherwise each chunk writes
-//   (m, l, unnormalised acc) to the workspace and the combine kernel merges them:
-//   O = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c.
-// Keys at positions >= ctx + 1 in the last block are excluded (score -inf, value unread).
+// * Balanced split: the 16-token blocks of all decode rows, concatenated in request
+//   order (page_off[r] = first global block of request r), are cut into gridDim.x equal
+//   contiguous ranges, one per CTA (one CTA per SM).  A CTA walks its range request by
+//   request; a request cut by a range boundary produces one partial per CTA that touches
+//   it (slot r + cta), merged afterwards by the combine kernel; a request inside one
+//   range is finished in place.  Every CTA streams the same number of blocks.
+// * One block of all 8 KV heads is 32 KiB contiguous in the pool, so each block of K and
+//   of V arrives with ONE bulk copy (cp.async.bulk, mbarrier completion, L2 evict-first)
+//   into a 3-stage shared-memory ring (64 KiB per stage).  Lane 0 of warp 0 issues the
+//   copies: after its warp has consumed a stage it refills it with the block three ahead.
+// * GQA packing: the 4 query heads of a KV head share every K/V byte read.  Two warps
+//   per KV head (16 warps) split each block's 16 tokens 8/8, with separate
+//   online-softmax states merged at the end of a request segment.
+// * Scores: a lane holds 16 of the 128 dims (8 lanes per token) of 2 tokens for all 4
+//   query heads; packed fp32x2 FMAs; a transpose-reduce over the 8 lanes (7 shuffles)
+//   leaves one finished (token, head) score per lane.  Online softmax in base 2 (the
+//   query is pre-scaled by softmax_scale * log2 e): running max m and sum l per head.
+// * P.V: a lane owns 4 output dims of all 4 heads; weights of the warp's 8 tokens go
+//   through a per-warp shared-memory slot as duplicated pairs for the packed FMAs.
+// Partial results keep (m, l, unnormalised acc); the combine is
+// O = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s with M = max_s m_s.
+// Keys at positions >= ctx + 1 of the last block are excluded (score -inf, value unread).
 #include "kvp_device.cuh"
 #include "kvp_launch.h"
 
@@ -32,18 +35,31 @@ namespace kvp {
 
 namespace {
 
-constexpr int kDecConsumerWarps = 16;
-constexpr int kDecThreads = (kDecConsumerWarps + 1) * 32;
+constexpr int kDecWarps = 16;
+constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDecStages = 3;
 constexpr int kTokensPerWarp = kBlockSize / 2;
 
+// Producer cursor over the CTA's blocks (used by lane 0 of warp 0 only; kept in shared
+// memory so the other 511 threads do not carry its registers).
+struct Producer {
+    int r, page, hi;
+    int stage;
+    uint32_t phase;
+    int issued;
+    int ok;
+    uint64_t policy;
+};
+
 struct __align__(128) DecodeSmem {
-    uint8_t kv[kDecStages][2][kBlockBytes];                 // [stage][K|V][8 heads x 16 x 128 bf16]
-    float4 pbuf[kDecConsumerWarps][kTokensPerWarp];          // softmax weights of 4 heads per token
-    float4 abuf[kDecConsumerWarps];                          // rescale factors of 4 heads
-    float merge_acc[kNumKvHeads][32][16];                    // second half's accumulators
-    float merge_ml[kNumKvHeads][8];                          // second half's m[4], l[4]
+    uint8_t kv[kDecStages][2][kBlockBytes];          // [stage][K|V][8 heads x 16 x 128 bf16]
+    float2 pbuf[kDecWarps][kTokensPerWarp][kGroup];   // (p, p) per token and head
+    float2 abuf[kDecWarps][kGroup];                   // (alpha, alpha) per head
+    float2 merge_acc[kNumKvHeads][32][8];             // second half's accumulators
+    float merge_ml[kNumKvHeads][8];                   // second half's m[4], l[4]
     int pair_abort[kNumKvHeads];
+    int first_req;
+    Producer prod;
     uint64_t full[kDecStages];
     uint64_t empty[kDecStages];
 };
@@ -52,191 +68,221 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
-    f[0] = bf16lo(u.x); f[1] = bf16hi(u.x);
-    f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
-    f[4] = bf16lo(u.z); f[5] = bf16hi(u.z);
-    f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
+
+// Partial dot products of one token's 16-dim slice (chunks dg and dg + 8 of its 256-byte
+// K row) with the 4 query heads' matching slices.
+__device__ __forceinline__ void token_scores(const float2 (&q2)[kGroup][8], const uint8_t* krow, int dg,
+                                             float (&v)[kGroup]) {
+    const uint4 ka = *reinterpret_cast<const uint4*>(krow + dg * 16);
+    const uint4 kb = *reinterpret_cast<const uint4*>(krow + 128 + dg * 16);
+    const uint32_t w[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+    float2 s[kGroup];
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) s[g] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float2 k = bf16x2_to_f2(w[i]);
+#pragma unroll
+        for (int g = 0; g < kGroup; ++g) s[g] = __ffma2_rn(q2[g][i], k, s[g]);
+    }
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) v[g] = s[g].x + s[g].y;
+}
+
+// Block range [lo, hi) of CTA c out of G over P blocks.
+__device__ __forceinline__ void cta_range(int P, int c, int G, int& lo, int& hi) {
+    lo = (int)(((long long)P * c) / G);
+    hi = (int)(((long long)P * (c + 1)) / G);
+}
+
+// The CTA whose range holds global block x.
+__device__ __forceinline__ int owner_cta(int x, int P, int G) {
+    return (int)((((long long)x + 1) * G - 1) / P);
+}
+
+
+__device__ __noinline__ void produce_next(DecodeSmem& S, const int32_t* __restrict__ page_off, int num_reqs,
+                                          const int32_t* __restrict__ tables, int max_blocks, int num_blocks,
+                                          const uint8_t* __restrict__ k_cache, const uint8_t* __restrict__ v_cache,
+                                          uint32_t* __restrict__ err) {
+    Producer& pr = S.prod;
+    if (!pr.ok || pr.page >= pr.hi) return;
+    const int req_lo = page_off[pr.r];
+    int b = tables[(size_t)pr.r * max_blocks + (pr.page - req_lo)];
+    if ((unsigned)b >= (unsigned)num_blocks) {
+        raise_error(err, kErrBadBlock);
+        b = 0;
+    }
+    if (!mbar_wait(&S.empty[pr.stage], pr.phase ^ 1)) {
+        raise_error(err, kErrTimeout);
+        pr.ok = 0;
+        return;
+    }
+    mbar_arrive_expect_tx(&S.full[pr.stage], 2 * kBlockBytes);
+    bulk_load(S.kv[pr.stage][0], k_cache + (size_t)b * kBlockBytes, kBlockBytes, &S.full[pr.stage], pr.policy);
+    bulk_load(S.kv[pr.stage][1], v_cache + (size_t)b * kBlockBytes, kBlockBytes, &S.full[pr.stage], pr.policy);
+    ++pr.issued;
+    if (++pr.stage == kDecStages) {
+        pr.stage = 0;
+        pr.phase ^= 1;
+    }
+    if (++pr.page < pr.hi) {
+        while (pr.r + 1 < num_reqs && page_off[pr.r + 1] <= pr.page) ++pr.r;
+    }
 }
 
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
     const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out, const int32_t* __restrict__ cu,
     const int32_t* __restrict__ ctx, const int32_t* __restrict__ tables, int max_blocks, int num_blocks,
-    const uint8_t* __restrict__ k_cache, const uint8_t* __restrict__ v_cache, const int32_t* __restrict__ counters,
-    const int4* __restrict__ items, float* __restrict__ part_acc, float2* __restrict__ part_ml, float scale_log2,
+    const uint8_t* __restrict__ k_cache, const uint8_t* __restrict__ v_cache, const int32_t* __restrict__ page_off,
+    int num_reqs, float* __restrict__ part_acc, float2* __restrict__ part_ml, float scale_log2,
     uint32_t* __restrict__ err) {
     extern __shared__ uint8_t smem_raw[];
     DecodeSmem& S = *reinterpret_cast<DecodeSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_items = counters[0];
-    if ((int)blockIdx.x >= n_items) return;
+    const int P = page_off[num_reqs];
+    int lo, hi;
+    cta_range(P, blockIdx.x, gridDim.x, lo, hi);
+    if (lo >= hi) return;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(&S.full[s], 1);
-            mbar_init(&S.empty[s], kDecConsumerWarps);
+            mbar_init(&S.empty[s], kDecWarps);
         }
         fence_barrier_init();
+        // request holding block lo: the last r with page_off[r] <= lo
+        int a = 0, b = num_reqs;  // page_off[a] <= lo < page_off[b]
+        while (b - a > 1) {
+            const int mid = (a + b) >> 1;
+            if (page_off[mid] <= lo) a = mid;
+            else b = mid;
+        }
+        S.first_req = a;
     }
     if (threadIdx.x < kNumKvHeads) S.pair_abort[threadIdx.x] = 0;
     __syncthreads();
 
-    if (warp == kDecConsumerWarps) {
-        // ---------------------------------------------------------------- producer
-        if (lane != 0) return;
-        const uint64_t pol = policy_evict_first();
-        int stage = 0;
-        uint32_t phase = 0;
-        int issued = 0;
-        bool ok = true;
-        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-            const int4 item = items[it];
-            const int32_t* trow = tables + (size_t)item.x * max_blocks + item.y;
-            for (int j = 0; j < item.z; ++j) {
-                int b = trow[j];
-                if ((unsigned)b >= (unsigned)num_blocks) {
-                    raise_error(err, kErrBadBlock);
-                    b = 0;
-                }
-                if (!mbar_wait(&S.empty[stage], phase ^ 1)) {
-                    raise_error(err, kErrTimeout);
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&S.full[stage], 2 * kBlockBytes);
-                bulk_load(S.kv[stage][0], k_cache + (size_t)b * kBlockBytes, kBlockBytes, &S.full[stage], pol);
-                bulk_load(S.kv[stage][1], v_cache + (size_t)b * kBlockBytes, kBlockBytes, &S.full[stage], pol);
-                ++issued;
-                if (++stage == kDecStages) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-            }
-        }
-        // Drain: the CTA must not retire while a copy still targets its shared memory.
-        for (int k = 1; k <= kDecStages && k <= issued; ++k) {
-            int s = stage - k;
-            uint32_t ph = phase;
-            if (s < 0) {
-                s += kDecStages;
-                ph ^= 1;
-            }
-            if (!mbar_wait(&S.full[s], ph)) raise_error(err, kErrTimeout);
-        }
-        return;
+    const bool is_producer = (warp == 0 && lane == 0);
+    if (is_producer) {
+        S.prod = Producer{S.first_req, lo, hi, 0, 0, 0, 1, policy_evict_first()};
+        for (int s = 0; s < kDecStages; ++s)
+            produce_next(S, page_off, num_reqs, tables, max_blocks, num_blocks, k_cache, v_cache, err);
     }
 
-    // -------------------------------------------------------------------- consumers
     const int h = warp >> 1, half = warp & 1;
-    const int dg = lane & 7;                 // 16-dim slice: dims 8dg..8dg+7 and 64+8dg..64+8dg+7
-    const int tl = lane >> 3;                // token within a pass of 4
-    const int hd = ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);  // head whose score this lane ends with
+    const int dg = lane & 7;                      // dims 8dg..8dg+7 and 64+8dg..64+8dg+7
+    const int tl = lane >> 3;                     // token within a group of 4
+    const int my_tok = (lane & 1) * 4 + tl;       // token (of the warp's 8) whose score this lane ends with
+    const int hd = ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);  // ... and its head
     int stage = 0;
     uint32_t phase = 0;
     bool aborted = false;
 
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const int4 item = items[it];
-        const int r = item.x, first_page = item.y, npages = item.z, slot = item.w;
+    int r = S.first_req;
+    int page = lo;
+    while (page < hi) {
+        const int req_lo = page_off[r], req_hi = page_off[r + 1];
+        const int seg_end = min(hi, req_hi);
+        const bool whole = (page == req_lo) && (seg_end == req_hi);
         const int row = cu[r];
         const int n_keys = ctx[r] + 1;
 
-        float qf[kGroup][16];
+        float2 q2[kGroup][8];
 #pragma unroll
         for (int g = 0; g < kGroup; ++g) {
             const uint4* qp = reinterpret_cast<const uint4*>(q + (size_t)row * kQRowElems + (h * kGroup + g) * kHeadDim);
-            float t[8];
-            bf16x8_to_f32(qp[dg], t);
+            const uint4 a = qp[dg], b = qp[8 + dg];
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) qf[g][i] = t[i] * scale_log2;
-            bf16x8_to_f32(qp[8 + dg], t);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) qf[g][8 + i] = t[i] * scale_log2;
+            for (int i = 0; i < 8; ++i) {
+                const float2 f = bf16x2_to_f2(w[i]);
+                q2[g][i] = make_float2(f.x * scale_log2, f.y * scale_log2);
+            }
         }
         float m_own = -INFINITY, l_own = 0.f;
-        float acc[kGroup][4];
+        float2 acc[kGroup][2];
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[g][i] = 0.f;
+        for (int g = 0; g < kGroup; ++g) acc[g][0] = acc[g][1] = make_float2(0.f, 0.f);
 
-        for (int j = 0; j < npages; ++j) {
+        for (; page < seg_end; ++page) {
             if (!aborted && !mbar_wait(&S.full[stage], phase)) {
                 raise_error(err, kErrTimeout);
                 aborted = true;
             }
             if (!aborted) {
-                const uint8_t* kt = S.kv[stage][0] + h * kTileBytes;
-                const uint8_t* vt = S.kv[stage][1] + h * kTileBytes;
-                const int pos0 = (first_page + j) * kBlockSize;
-                float sc[2];
+                const uint8_t* kt = S.kv[stage][0] + h * kTileBytes + half * kTokensPerWarp * kHeadBytes;
+                const uint8_t* vt = S.kv[stage][1] + h * kTileBytes + half * kTokensPerWarp * kHeadBytes;
+                const int pos0 = (page - req_lo) * kBlockSize + half * kTokensPerWarp;
+                const int n_valid = min(kTokensPerWarp, n_keys - pos0);   // >= 1 except in a last block
+                // ---- scores of tokens tl and 4 + tl, all 4 heads
+                const uint8_t* k0 = kt + tl * kHeadBytes;
+                float v0[kGroup], v1[kGroup];
+                token_scores(q2, k0, dg, v0);
+                token_scores(q2, k0 + 4 * kHeadBytes, dg, v1);
+                // transpose-reduce over the 8 lanes of a token: bit 2 picks the head pair,
+                // bit 1 the head, bit 0 the token
+                const bool b2 = (lane >> 2) & 1, b1 = (lane >> 1) & 1, b0 = lane & 1;
+                float x[4], y[4];
+                x[0] = b2 ? v0[2] : v0[0];
+                x[1] = b2 ? v0[3] : v0[1];
+                x[2] = b2 ? v1[2] : v1[0];
+                x[3] = b2 ? v1[3] : v1[1];
+                y[0] = b2 ? v0[0] : v0[2];
+                y[1] = b2 ? v0[1] : v0[3];
+                y[2] = b2 ? v1[0] : v1[2];
+                y[3] = b2 ? v1[1] : v1[3];
 #pragma unroll
-                for (int a = 0; a < 2; ++a) {
-                    const int tok = half * kTokensPerWarp + a * 4 + tl;
-                    const uint4 k0 = *reinterpret_cast<const uint4*>(kt + tok * kHeadBytes + dg * 16);
-                    const uint4 k1 = *reinterpret_cast<const uint4*>(kt + tok * kHeadBytes + 128 + dg * 16);
-                    float kf[16];
-                    bf16x8_to_f32(k0, kf);
-                    bf16x8_to_f32(k1, kf + 8);
-                    float v[kGroup];
-#pragma unroll
-                    for (int g = 0; g < kGroup; ++g) {
-                        float s = 0.f;
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) s = fmaf(qf[g][i], kf[i], s);
-                        v[g] = s;
-                    }
-                    // transpose-reduce over the 8 lanes of this token
-                    const bool b2 = (lane >> 2) & 1;
-                    float k_lo = b2 ? v[2] : v[0], k_hi = b2 ? v[3] : v[1];
-                    const float s_lo = b2 ? v[0] : v[2], s_hi = b2 ? v[1] : v[3];
-                    k_lo += __shfl_xor_sync(0xffffffffu, s_lo, 4);
-                    k_hi += __shfl_xor_sync(0xffffffffu, s_hi, 4);
-                    const bool b1 = (lane >> 1) & 1;
-                    float kk = b1 ? k_hi : k_lo;
-                    kk += __shfl_xor_sync(0xffffffffu, b1 ? k_lo : k_hi, 2);
-                    kk += __shfl_xor_sync(0xffffffffu, kk, 1);
-                    sc[a] = (pos0 + tok < n_keys) ? kk : -INFINITY;
-                }
-                float mx = fmaxf(sc[0], sc[1]);
+                for (int k = 0; k < 4; ++k) x[k] += __shfl_xor_sync(0xffffffffu, y[k], 4);
+                float u0 = b1 ? x[1] : x[0], u1 = b1 ? x[3] : x[2];
+                const float t0 = b1 ? x[0] : x[1], t1 = b1 ? x[2] : x[3];
+                u0 += __shfl_xor_sync(0xffffffffu, t0, 2);
+                u1 += __shfl_xor_sync(0xffffffffu, t1, 2);
+                float sc = b0 ? u1 : u0;
+                sc += __shfl_xor_sync(0xffffffffu, b0 ? u0 : u1, 1);
+                if (my_tok >= n_valid) sc = -INFINITY;
+                // ---- online softmax for head hd over the warp's 8 tokens
+                float mx = sc;
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 const float m_new = fmaxf(m_own, mx);
                 const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
                 const float alpha = fast_exp2(m_own - m_use);
-                const float p0 = fast_exp2(sc[0] - m_use), p1 = fast_exp2(sc[1] - m_use);
-                float ps = p0 + p1;
+                const float p = fast_exp2(sc - m_use);
+                float ps = p;
+                ps += __shfl_xor_sync(0xffffffffu, ps, 1);
                 ps += __shfl_xor_sync(0xffffffffu, ps, 8);
                 ps += __shfl_xor_sync(0xffffffffu, ps, 16);
                 l_own = l_own * alpha + ps;
                 m_own = m_new;
-                float* pw = reinterpret_cast<float*>(&S.pbuf[warp][0]);
-                if ((lane & 1) == 0) {
-                    pw[tl * 4 + hd] = p0;
-                    pw[(4 + tl) * 4 + hd] = p1;
-                }
-                if ((lane & 0x19) == 0) reinterpret_cast<float*>(&S.abuf[warp])[hd] = alpha;
+                S.pbuf[warp][my_tok][hd] = make_float2(p, p);
+                if ((lane & 0x19) == 0) S.abuf[warp][hd] = make_float2(alpha, alpha);
                 __syncwarp();
-                const float4 al = S.abuf[warp];
-                const float alv[4] = {al.x, al.y, al.z, al.w};
+                // ---- rescale and accumulate P.V (lane owns dims 4*lane .. 4*lane+3)
+                const float4 al01 = *reinterpret_cast<const float4*>(&S.abuf[warp][0]);
+                const float4 al23 = *reinterpret_cast<const float4*>(&S.abuf[warp][2]);
+                const float2 al[4] = {make_float2(al01.x, al01.y), make_float2(al01.z, al01.w),
+                                      make_float2(al23.x, al23.y), make_float2(al23.z, al23.w)};
 #pragma unroll
-                for (int g = 0; g < kGroup; ++g)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[g][i] *= alv[g];
+                for (int g = 0; g < kGroup; ++g) {
+                    acc[g][0] = __fmul2_rn(acc[g][0], al[g]);
+                    acc[g][1] = __fmul2_rn(acc[g][1], al[g]);
+                }
 #pragma unroll
                 for (int t = 0; t < kTokensPerWarp; ++t) {
-                    const int tok = half * kTokensPerWarp + t;
-                    if (pos0 + tok < n_keys) {
-                        const uint2 vv = *reinterpret_cast<const uint2*>(vt + tok * kHeadBytes + lane * 8);
-                        const float v0 = bf16lo(vv.x), v1 = bf16hi(vv.x), v2 = bf16lo(vv.y), v3 = bf16hi(vv.y);
-                        const float4 pp = S.pbuf[warp][t];
-                        const float pg[4] = {pp.x, pp.y, pp.z, pp.w};
+                    if (t < n_valid) {
+                        const uint2 vv = *reinterpret_cast<const uint2*>(vt + t * kHeadBytes + lane * 8);
+                        const float2 va = bf16x2_to_f2(vv.x), vb = bf16x2_to_f2(vv.y);
+                        const float4 p01 = *reinterpret_cast<const float4*>(&S.pbuf[warp][t][0]);
+                        const float4 p23 = *reinterpret_cast<const float4*>(&S.pbuf[warp][t][2]);
+                        const float2 pg[4] = {make_float2(p01.x, p01.y), make_float2(p01.z, p01.w),
+                                              make_float2(p23.x, p23.y), make_float2(p23.z, p23.w)};
 #pragma unroll
                         for (int g = 0; g < kGroup; ++g) {
-                            acc[g][0] = fmaf(pg[g], v0, acc[g][0]);
-                            acc[g][1] = fmaf(pg[g], v1, acc[g][1]);
-                            acc[g][2] = fmaf(pg[g], v2, acc[g][2]);
-                            acc[g][3] = fmaf(pg[g], v3, acc[g][3]);
+                            acc[g][0] = __ffma2_rn(va, pg[g], acc[g][0]);
+                            acc[g][1] = __ffma2_rn(vb, pg[g], acc[g][1]);
                         }
                     }
                 }
@@ -247,6 +293,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
                 stage = 0;
                 phase ^= 1;
             }
+            if (is_producer) produce_next(S, page_off, num_reqs, tables, max_blocks, num_blocks, k_cache, v_cache, err);
         }
 
         // ------------------------------------------------ merge the two token halves
@@ -260,9 +307,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
         if (aborted && lane == 0) S.pair_abort[h] = 1;
         if (half == 1) {
 #pragma unroll
-            for (int g = 0; g < kGroup; ++g)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) S.merge_acc[h][lane][g * 4 + i] = acc[g][i];
+            for (int g = 0; g < kGroup; ++g) {
+                S.merge_acc[h][lane][2 * g] = acc[g][0];
+                S.merge_acc[h][lane][2 * g + 1] = acc[g][1];
+            }
             if (lane == 0) {
 #pragma unroll
                 for (int g = 0; g < kGroup; ++g) {
@@ -281,87 +329,109 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
                 const float Mu = (M == -INFINITY) ? 0.f : M;
                 const float e0 = fast_exp2(m[g] - Mu), e1 = fast_exp2(m1 - Mu);
                 const float L = l[g] * e0 + l1 * e1;
-                float o[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) o[i] = acc[g][i] * e0 + S.merge_acc[h][lane][g * 4 + i] * e1;
+                const float2 b0 = S.merge_acc[h][lane][2 * g], b1 = S.merge_acc[h][lane][2 * g + 1];
+                const float o0 = acc[g][0].x * e0 + b0.x * e1, o1 = acc[g][0].y * e0 + b0.y * e1;
+                const float o2 = acc[g][1].x * e0 + b1.x * e1, o3 = acc[g][1].y * e0 + b1.y * e1;
                 const int head = h * kGroup + g;
-                if (slot < 0) {
+                if (whole) {
                     const float inv = L > 0.f ? 1.f / L : 0.f;
-                    uint2 w;
-                    w.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-                    w.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-                    *reinterpret_cast<uint2*>(out + (size_t)row * kQRowElems + head * kHeadDim + lane * 4) = w;
+                    uint2 wv;
+                    wv.x = pack_bf16x2(o0 * inv, o1 * inv);
+                    wv.y = pack_bf16x2(o2 * inv, o3 * inv);
+                    *reinterpret_cast<uint2*>(out + (size_t)row * kQRowElems + head * kHeadDim + lane * 4) = wv;
                 } else {
-                    *reinterpret_cast<float4*>(part_acc + ((size_t)slot * kNumQHeads + head) * kHeadDim + lane * 4) =
-                        make_float4(o[0], o[1], o[2], o[3]);
-                    if (lane == 0) part_ml[(size_t)slot * kNumQHeads + head] = make_float2(M, L);
+                    const size_t slot = (size_t)r + blockIdx.x;
+                    *reinterpret_cast<float4*>(part_acc + (slot * kNumQHeads + head) * kHeadDim + lane * 4) =
+                        make_float4(o0, o1, o2, o3);
+                    if (lane == 0) part_ml[slot * kNumQHeads + head] = make_float2(M, L);
                 }
             }
         }
         named_bar(1 + h, 64);
         if (pair_aborted) break;
+        // next request that has blocks
+        ++r;
+        while (r + 1 <= num_reqs - 1 && page_off[r + 1] == page_off[r]) ++r;
+    }
+
+    if (is_producer) {
+        // Drain: the CTA must not retire while a copy still targets its shared memory.
+        const Producer& pr = S.prod;
+        for (int k = 1; k <= kDecStages && k <= pr.issued; ++k) {
+            int s = pr.stage - k;
+            uint32_t ph = pr.phase;
+            if (s < 0) {
+                s += kDecStages;
+                ph ^= 1;
+            }
+            if (!mbar_wait(&S.full[s], ph)) raise_error(err, kErrTimeout);
+        }
     }
 }
 
-// Merge the split-KV partials of one decode row: one warp per (request, query head),
-// a lane owns 4 output dims.
-__global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict__ counters,
-                                                      const int4* __restrict__ combines,
+// Merge the partials of decode rows whose blocks were split across CTAs: one CTA per
+// (request, group of 8 query heads), one warp per query head, a lane owns 4 dims.
+__global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict__ page_off, int num_reqs, int G,
                                                       const int32_t* __restrict__ cu,
                                                       const float* __restrict__ part_acc,
                                                       const float2* __restrict__ part_ml,
                                                       __nv_bfloat16* __restrict__ out) {
-    const int e = blockIdx.x;
-    if (e >= counters[2]) return;
+    const int r = blockIdx.x;
+    const int P = page_off[num_reqs];
+    const int a = page_off[r], b = page_off[r + 1];
+    if (b <= a) return;
+    const int c0 = owner_cta(a, P, G), c1 = owner_cta(b - 1, P, G);
+    if (c0 == c1) return;  // finished in place by its CTA
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int head = blockIdx.y * 8 + warp;
-    const int4 c = combines[e];
-    const int row = cu[c.x];
     float M = -INFINITY;
-    for (int k = 0; k < c.z; ++k) M = fmaxf(M, part_ml[(size_t)(c.y + k) * kNumQHeads + head].x);
+    for (int c = c0; c <= c1; ++c) M = fmaxf(M, part_ml[((size_t)r + c) * kNumQHeads + head].x);
     const float Mu = (M == -INFINITY) ? 0.f : M;
     float L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-    for (int k = 0; k < c.z; ++k) {
-        const size_t sh = (size_t)(c.y + k) * kNumQHeads + head;
+    for (int c = c0; c <= c1; ++c) {
+        const size_t sh = ((size_t)r + c) * kNumQHeads + head;
         const float2 ml = part_ml[sh];
         const float w = fast_exp2(ml.x - Mu);
         L = fmaf(ml.y, w, L);
-        const float4 a = *reinterpret_cast<const float4*>(part_acc + sh * kHeadDim + lane * 4);
-        o0 = fmaf(a.x, w, o0);
-        o1 = fmaf(a.y, w, o1);
-        o2 = fmaf(a.z, w, o2);
-        o3 = fmaf(a.w, w, o3);
+        const float4 v = *reinterpret_cast<const float4*>(part_acc + sh * kHeadDim + lane * 4);
+        o0 = fmaf(v.x, w, o0);
+        o1 = fmaf(v.y, w, o1);
+        o2 = fmaf(v.z, w, o2);
+        o3 = fmaf(v.w, w, o3);
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     uint2 wv;
     wv.x = pack_bf16x2(o0 * inv, o1 * inv);
     wv.y = pack_bf16x2(o2 * inv, o3 * inv);
-    *reinterpret_cast<uint2*>(out + (size_t)row * kQRowElems + head * kHeadDim + lane * 4) = wv;
+    *reinterpret_cast<uint2*>(out + (size_t)cu[r] * kQRowElems + head * kHeadDim + lane * 4) = wv;
+}
+
+int decode_grid(const StepArgs& a) {
+    int g = a.num_sms > 0 ? a.num_sms : 1;
+    if (g > kMaxDecodeCtas) g = kMaxDecodeCtas;
+    if (a.decode_ctas > 0 && a.decode_ctas < g) g = a.decode_ctas;
+    return g;
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream) {
     const StepLayout& L = a.lay;
-    if (L.max_decode_items <= 0) return cudaSuccess;
-    int grid = a.num_sms;
-    if (grid > L.max_decode_items) grid = L.max_decode_items;
     const size_t smem = sizeof(DecodeSmem) + 128;
-    decode_kernel<<<grid, kDecThreads, smem, stream>>>(
+    decode_kernel<<<decode_grid(a), kDecThreads, smem, stream>>>(
         static_cast<const __nv_bfloat16*>(a.q), static_cast<__nv_bfloat16*>(a.out), a.cu_seqlens_q, a.context_lens,
         a.block_tables, a.max_blocks_per_seq, a.num_blocks, static_cast<const uint8_t*>(a.k_cache),
-        static_cast<const uint8_t*>(a.v_cache), reinterpret_cast<const int32_t*>(a.ws + L.counters_off),
-        reinterpret_cast<const int4*>(a.ws + L.decode_items_off), reinterpret_cast<float*>(a.ws + L.part_acc_off),
-        reinterpret_cast<float2*>(a.ws + L.part_ml_off), a.softmax_scale * 1.4426950408889634f, a.err);
+        static_cast<const uint8_t*>(a.v_cache), reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs,
+        reinterpret_cast<float*>(a.ws + L.part_acc_off), reinterpret_cast<float2*>(a.ws + L.part_ml_off),
+        a.softmax_scale * 1.4426950408889634f, a.err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const StepArgs& a, cudaStream_t stream) {
     const StepLayout& L = a.lay;
-    if (L.max_combines <= 0) return cudaSuccess;
-    dim3 grid(L.max_combines, kNumQHeads / 8);
-    combine_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const int32_t*>(a.ws + L.counters_off),
-                                             reinterpret_cast<const int4*>(a.ws + L.combines_off), a.cu_seqlens_q,
+    dim3 grid(a.num_reqs, kNumQHeads / 8);
+    combine_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs,
+                                             decode_grid(a), a.cu_seqlens_q,
                                              reinterpret_cast<const float*>(a.ws + L.part_acc_off),
                                              reinterpret_cast<const float2*>(a.ws + L.part_ml_off),
                                              static_cast<__nv_bfloat16*>(a.out));

@@ -5,9 +5,11 @@
 // offset p % 16.  The pool keeps each (block, KV head) tile of 16 x 128 bf16 contiguous,
 // so one (row, head) write is a single 256-byte run: 16 lanes each store 16 bytes.
 //
-// One CTA of 256 threads per packed row: threads 0..127 move K, 128..255 move V; within
-// each half, thread t handles head t / 16 and 16-byte chunk t % 16.  Loads of the new row
-// are fully coalesced (2 KiB per tensor per row); stores are 256-byte runs per head.
+// One CTA of 256 threads per packed row: the threads first look the row's request up in
+// cu_seqlens together (one round of loads instead of a serial binary search), then
+// threads 0..127 move K and 128..255 move V; within each half, thread t handles head
+// t / 16 and 16-byte chunk t % 16.  Loads of the new row are fully coalesced (2 KiB per
+// tensor per row); stores are 256-byte runs per head.
 #include "kvp_device.cuh"
 #include "kvp_launch.h"
 
@@ -23,23 +25,22 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
                                                         const int32_t* __restrict__ refcnt, int num_blocks,
                                                         uint32_t* __restrict__ err) {
     __shared__ long long s_dst;  // element-chunk index of (block, head 0, slot) or -1
+    __shared__ int s_req;
     const int i = blockIdx.x;
+    if (threadIdx.x == 0) s_req = -1;
+    __syncthreads();
+    // request r with cu[r] <= i < cu[r+1]: all threads test requests in parallel
+    for (int r = threadIdx.x; r < num_reqs; r += blockDim.x)
+        if (cu[r] <= i && i < cu[r + 1]) s_req = r;
+    __syncthreads();
     if (threadIdx.x == 0) {
         long long dst = -1;
-        // request r with cu[r] <= i < cu[r+1] (binary search; checked afterwards)
-        int lo = 0, hi = num_reqs;  // answer in [lo, hi)
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (cu[mid] <= i) lo = mid;
-            else hi = mid;
-        }
-        const int r = lo;
-        const int c0 = cu[r], c1 = cu[r + 1];
-        if (num_reqs <= 0 || !(c0 <= i && i < c1)) {
+        const int r = s_req;
+        if (r < 0) {
             raise_error(err, kErrBadMeta);
         } else {
             const int cl = ctx[r];
-            const long long p = (long long)cl + (i - c0);
+            const long long p = (long long)cl + (i - cu[r]);
             const long long lb = p >> 4;
             if (cl < 0 || lb >= max_blocks) {
                 raise_error(err, kErrBadMeta);

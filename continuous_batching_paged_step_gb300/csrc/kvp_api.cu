@@ -26,7 +26,7 @@ struct kvp_pool {
     std::vector<int32_t> free_pos;   // index in free_list, -1 when allocated
     std::vector<int32_t> refcnt;
     int dirty_lo = 1, dirty_hi = 0;  // refcount range changed since the last upload
-    int decode_chunk_pages = 32;
+    int decode_ctas = 0;  // 0: one decode CTA per SM
     // device state (made on first device call)
     int device = -1;
     int num_sms = 0;
@@ -305,9 +305,9 @@ int kv_block_refcount(const kvp_pool* p, int32_t id) {
     return p->refcnt[id];
 }
 
-kvp_status kv_pool_set_decode_split(kvp_pool* p, int pages) {
-    if (!p || pages < 1 || pages > 4096) return KVP_E_INVALID_ARG;
-    p->decode_chunk_pages = pages;
+kvp_status kv_pool_set_decode_ctas(kvp_pool* p, int ctas) {
+    if (!p || ctas < 0 || ctas > kvp::kMaxDecodeCtas) return KVP_E_INVALID_ARG;
+    p->decode_ctas = ctas;
     return KVP_OK;
 }
 
@@ -334,7 +334,7 @@ kvp_status kv_append(kvp_pool* p, const void* k_new, const void* v_new, const in
 size_t paged_attention_workspace_size(const kvp_pool* p, int num_reqs, int num_tokens, int n_q_heads,
                                       int max_context_len) {
     if (!p || num_reqs < 0 || num_tokens < 0 || max_context_len < 0 || n_q_heads != kvp::kNumQHeads) return 0;
-    return kvp::make_step_layout(num_reqs, num_tokens, max_context_len, p->decode_chunk_pages).total;
+    return kvp::make_step_layout(num_reqs, num_tokens).total;
 }
 
 kvp_status paged_attention_step(kvp_pool* p, const void* q, void* out, const int32_t* cu_seqlens_q,
@@ -347,7 +347,7 @@ kvp_status paged_attention_step(kvp_pool* p, const void* q, void* out, const int
         !cu_seqlens_q || !context_lens || !block_tables || !aligned16(q) || !aligned16(out) ||
         !(softmax_scale > 0.f))
         return KVP_E_INVALID_ARG;
-    kvp::StepLayout lay = kvp::make_step_layout(num_reqs, num_tokens, max_context_len, p->decode_chunk_pages);
+    kvp::StepLayout lay = kvp::make_step_layout(num_reqs, num_tokens);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < lay.total)
         return KVP_E_WORKSPACE;
     kvp_status st = ensure_device(p);
@@ -372,6 +372,7 @@ kvp_status paged_attention_step(kvp_pool* p, const void* q, void* out, const int
     a.ws = static_cast<char*>(workspace);
     a.lay = lay;
     a.num_sms = p->num_sms;
+    a.decode_ctas = p->decode_ctas;
     if (timed_launch(p, KVP_KERNEL_PREP, s, [&] { return kvp::launch_step_prep(a, s); }) != cudaSuccess)
         return KVP_E_CUDA;
     if (max_q_len >= 2 && lay.max_prefill_tiles > 0) {
@@ -381,11 +382,9 @@ kvp_status paged_attention_step(kvp_pool* p, const void* q, void* out, const int
                          [&] { return kvp::launch_prefill(a, &tq, &p->tmap_k, &p->tmap_v, s); }) != cudaSuccess)
             return KVP_E_CUDA;
     }
-    if (lay.max_decode_items > 0 &&
-        timed_launch(p, KVP_KERNEL_DECODE, s, [&] { return kvp::launch_decode(a, s); }) != cudaSuccess)
+    if (timed_launch(p, KVP_KERNEL_DECODE, s, [&] { return kvp::launch_decode(a, s); }) != cudaSuccess)
         return KVP_E_CUDA;
-    if (lay.max_combines > 0 &&
-        timed_launch(p, KVP_KERNEL_COMBINE, s, [&] { return kvp::launch_combine(a, s); }) != cudaSuccess)
+    if (timed_launch(p, KVP_KERNEL_COMBINE, s, [&] { return kvp::launch_combine(a, s); }) != cudaSuccess)
         return KVP_E_CUDA;
     return KVP_OK;
 }

@@ -11,21 +11,20 @@ namespace kvp {
 // Scratch layout inside the caller's workspace for one paged_attention_step call.
 // Offsets are in bytes from the workspace base; every region is 256-byte aligned.
 struct StepLayout {
-    int max_decode_items;    // (request, chunk of pages) work items of decode rows
-    int max_partials;        // split-KV partial slots (requests with more than one chunk)
     int max_prefill_tiles;   // (request, 32-token q tile) work items of prefill chunks
-    int max_combines;        // decode requests whose chunks are merged
-    int decode_chunk_pages;
-    size_t counters_off;     // int32[8]: 0 decode items, 1 prefill tiles, 2 combines
-    size_t decode_items_off; // int4 {r, first_page, n_pages, partial slot or -1}
+    int max_partials;        // split-KV partial slots: request r cut by CTA c uses r + c
+    size_t counters_off;     // int32[8]: 1 = prefill tiles
+    size_t page_off_off;     // int32 [num_reqs + 1]: first global decode block of each request
     size_t prefill_tiles_off;// int4 {r, first token of tile, tokens in tile, 0}
-    size_t combines_off;     // int4 {r, first slot, n_chunks, 0}
     size_t part_acc_off;     // float [slot][32 heads][128]  (unnormalised)
     size_t part_ml_off;      // float2 [slot][32 heads]      (running max (log2 units), sum)
     size_t total;
 };
 
-StepLayout make_step_layout(int num_reqs, int num_tokens, int max_context_len, int decode_chunk_pages);
+// Upper bound of the decode grid (CTAs that share out the decode blocks).
+constexpr int kMaxDecodeCtas = 1024;
+
+StepLayout make_step_layout(int num_reqs, int num_tokens);
 
 struct StepArgs {
     const void* q;
@@ -46,6 +45,7 @@ struct StepArgs {
     char* ws;
     StepLayout lay;
     int num_sms;
+    int decode_ctas;   // 0: one CTA per SM
 };
 
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t* cu, const int32_t* ctx,

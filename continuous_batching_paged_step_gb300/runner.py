@@ -27,7 +27,7 @@ def _dev_i32(a: np.ndarray, device) -> torch.Tensor:
 
 class PagedStep:
     def __init__(self, inp: StepInputs, device="cuda", pool_fill_bits: int | None = None,
-                 decode_split_pages: int | None = None, fill_prior: bool = True):
+                 decode_ctas: int | None = None, fill_prior: bool = True):
         spec = inp.spec
         self.inp = inp
         self.device = device
@@ -36,8 +36,8 @@ class PagedStep:
             fill = int(np.array([pool_fill_bits], dtype=np.uint16).view(np.int16)[0])
             self.pool.k_cache.view(torch.int16).fill_(fill)
             self.pool.v_cache.view(torch.int16).fill_(fill)
-        if decode_split_pages is not None:
-            kp.kv_pool_set_decode_split(self.pool.handle, decode_split_pages)
+        if decode_ctas is not None:
+            kp.kv_pool_set_decode_ctas(self.pool.handle, decode_ctas)
         kp.kv_block_claim(self.pool.handle, inp.block_order)
         self.block_tables = _dev_i32(inp.block_tables, device)
         self.cu_seqlens_q = _dev_i32(inp.cu_seqlens_q, device)

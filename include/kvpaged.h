@@ -183,10 +183,11 @@ KVP_API kvp_status paged_attention_step(kvp_pool* pool, const void* q, void* out
                                 int max_context_len, float softmax_scale, void* workspace,
                                 size_t workspace_bytes, kvp_stream stream);
 
-/* Decode split size: a decode row's history is cut into chunks of `pages` 16-token
- * blocks, each chunk handled by one CTA, and the partial results are merged.
- * 1 <= pages <= 4096; default 32.  Host-only. */
-KVP_API kvp_status kv_pool_set_decode_split(kvp_pool* pool, int pages);
+/* Decode split: the 16-token blocks of all decode rows of a step are shared out evenly,
+ * in request order, among `ctas` CTAs (0 = one per SM, the default; at most 1024); a
+ * row whose blocks fall to several CTAs is finished by a merge of their partial results.
+ * The workspace size does not depend on this setting.  Host-only. */
+KVP_API kvp_status kv_pool_set_decode_ctas(kvp_pool* pool, int ctas);
 
 /* Synchronise `stream`, then read and clear the pool's device error word.  *bits (may be
  * NULL) receives the KVP_ERRBIT_* mask; the return value is KVP_OK for an empty word,

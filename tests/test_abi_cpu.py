@@ -148,10 +148,11 @@ def test_workspace_size_and_split_setting(kp):
         small = kp.paged_attention_workspace_size(p, 3, 7, 7)
         big = kp.paged_attention_workspace_size(p, 300, 8224, 8192)
         assert 0 < small < big and small % 256 == 0
-        kp.kv_pool_set_decode_split(p, 1)
-        assert kp.paged_attention_workspace_size(p, 300, 8224, 8192) > big
-        with pytest.raises(kp.KVPError):
-            kp.kv_pool_set_decode_split(p, 0)
+        kp.kv_pool_set_decode_ctas(p, 5)
+        assert kp.paged_attention_workspace_size(p, 300, 8224, 8192) == big
+        for bad in (-1, 1025):
+            with pytest.raises(kp.KVPError):
+                kp.kv_pool_set_decode_ctas(p, bad)
         assert kp.lib.paged_attention_workspace_size(p, 3, 7, 16, 7) == 0     # only 32 query heads
     finally:
         kp.kv_pool_destroy(p)

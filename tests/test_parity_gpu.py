@@ -57,9 +57,9 @@ def _pool_bits(step):
     return k, v
 
 
-def _run_full_check(runner, spec, split=None):
+def _run_full_check(runner, spec, ctas=None):
     inp = wl.make_inputs(spec)
-    step = runner.PagedStep(inp, pool_fill_bits=NAN_BITS, decode_split_pages=split)
+    step = runner.PagedStep(inp, pool_fill_bits=NAN_BITS, decode_ctas=ctas)
     try:
         step.run()
         st, bits = step.error()
@@ -84,10 +84,12 @@ def test_small_mixed_step_all_rows(runner):
     _run_full_check(runner, wl.small_mixed_step())
 
 
-@pytest.mark.parametrize("split", [1, 3, 32])
-def test_decode_split_and_combine(runner, split):
+@pytest.mark.parametrize("ctas", [1, 7, 0, 1024])
+def test_decode_split_and_combine(runner, ctas):
+    # one CTA (no split), a few CTAs (most rows split across two), one per SM, and more
+    # CTAs than blocks (every row split block by block; idle CTAs)
     spec = wl.small_mixed_step(seed=77, n_decode=20, chunks=(), ctx_range=(0, 1500), num_blocks=4096)
-    _run_full_check(runner, spec, split=split)
+    _run_full_check(runner, spec, ctas=ctas)
 
 
 def test_edge_cases(runner):
