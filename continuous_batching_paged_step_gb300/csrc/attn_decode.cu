@@ -90,6 +90,23 @@ __device__ __forceinline__ void token_scores(const float2 (&q2)[kGroup][8], cons
     for (int g = 0; g < kGroup; ++g) v[g] = s[g].x + s[g].y;
 }
 
+// acc[g] += p[g] * v for one token: v is the lane's 4 dims of the token's V row, p the
+// token's weight for each of the 4 query heads (stored as duplicated pairs).
+__device__ __forceinline__ void pv_token(const float2 (&pt)[kGroup], const uint8_t* vrow, int lane,
+                                         float2 (&acc)[kGroup][2]) {
+    const uint2 vv = *reinterpret_cast<const uint2*>(vrow + lane * 8);
+    const float2 va = bf16x2_to_f2(vv.x), vb = bf16x2_to_f2(vv.y);
+    const float4 p01 = *reinterpret_cast<const float4*>(&pt[0]);
+    const float4 p23 = *reinterpret_cast<const float4*>(&pt[2]);
+    const float2 pg[4] = {make_float2(p01.x, p01.y), make_float2(p01.z, p01.w), make_float2(p23.x, p23.y),
+                          make_float2(p23.z, p23.w)};
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+        acc[g][0] = __ffma2_rn(va, pg[g], acc[g][0]);
+        acc[g][1] = __ffma2_rn(vb, pg[g], acc[g][1]);
+    }
+}
+
 // Block range [lo, hi) of CTA c out of G over P blocks.
 __device__ __forceinline__ void cta_range(int P, int c, int G, int& lo, int& hi) {
     lo = (int)(((long long)P * c) / G);
@@ -261,30 +278,22 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
                 if ((lane & 0x19) == 0) S.abuf[warp][hd] = make_float2(alpha, alpha);
                 __syncwarp();
                 // ---- rescale and accumulate P.V (lane owns dims 4*lane .. 4*lane+3)
-                const float4 al01 = *reinterpret_cast<const float4*>(&S.abuf[warp][0]);
-                const float4 al23 = *reinterpret_cast<const float4*>(&S.abuf[warp][2]);
-                const float2 al[4] = {make_float2(al01.x, al01.y), make_float2(al01.z, al01.w),
-                                      make_float2(al23.x, al23.y), make_float2(al23.z, al23.w)};
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                    const float4 al01 = *reinterpret_cast<const float4*>(&S.abuf[warp][0]);
+                    const float4 al23 = *reinterpret_cast<const float4*>(&S.abuf[warp][2]);
+                    const float2 al[4] = {make_float2(al01.x, al01.y), make_float2(al01.z, al01.w),
+                                          make_float2(al23.x, al23.y), make_float2(al23.z, al23.w)};
 #pragma unroll
-                for (int g = 0; g < kGroup; ++g) {
-                    acc[g][0] = __fmul2_rn(acc[g][0], al[g]);
-                    acc[g][1] = __fmul2_rn(acc[g][1], al[g]);
-                }
-#pragma unroll
-                for (int t = 0; t < kTokensPerWarp; ++t) {
-                    if (t < n_valid) {
-                        const uint2 vv = *reinterpret_cast<const uint2*>(vt + t * kHeadBytes + lane * 8);
-                        const float2 va = bf16x2_to_f2(vv.x), vb = bf16x2_to_f2(vv.y);
-                        const float4 p01 = *reinterpret_cast<const float4*>(&S.pbuf[warp][t][0]);
-                        const float4 p23 = *reinterpret_cast<const float4*>(&S.pbuf[warp][t][2]);
-                        const float2 pg[4] = {make_float2(p01.x, p01.y), make_float2(p01.z, p01.w),
-                                              make_float2(p23.x, p23.y), make_float2(p23.z, p23.w)};
-#pragma unroll
-                        for (int g = 0; g < kGroup; ++g) {
-                            acc[g][0] = __ffma2_rn(va, pg[g], acc[g][0]);
-                            acc[g][1] = __ffma2_rn(vb, pg[g], acc[g][1]);
-                        }
+                    for (int g = 0; g < kGroup; ++g) {
+                        acc[g][0] = __fmul2_rn(acc[g][0], al[g]);
+                        acc[g][1] = __fmul2_rn(acc[g][1], al[g]);
                     }
+                }
+                if (n_valid == kTokensPerWarp) {
+#pragma unroll
+                    for (int t = 0; t < kTokensPerWarp; ++t) pv_token(S.pbuf[warp][t], vt + t * kHeadBytes, lane, acc);
+                } else {
+                    for (int t = 0; t < n_valid; ++t) pv_token(S.pbuf[warp][t], vt + t * kHeadBytes, lane, acc);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.empty[stage]);

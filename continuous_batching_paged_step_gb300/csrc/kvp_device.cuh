@@ -76,15 +76,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 
 // Wait for the phase with the given parity to complete.  Returns false (and leaves
 // the barrier alone) if it has not completed within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    const uint32_t a = smem_u32(bar);
-    if (mbar_try_wait(a, parity)) return true;
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity) {
     const uint64_t t0 = global_ns();
     while (true) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(a, parity)) return true;
         if (global_ns() - t0 > kWaitLimitNs) return false;
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    return mbar_wait_slow(a, parity);
 }
 
 // ---------------------------------------------------------------- bulk / TMA copies
