@@ -4,29 +4,31 @@
 // rows, causally (page "Continuous Batching 深入实现", section "第三层：Chunked Prefill";
 // page "11.2 连续批处理与 PagedAttention", section 11.2.2, Figure 11-3: per head the
 // scores are Q[q, 128] x K^T[128, ctx + q] with a causal mask).  These are dense
-// contractions, so they run as tcgen05.mma (bf16 operands in shared memory, fp32
-// accumulators in TMEM).
+// contractions, so they run as tcgen05.mma (bf16 operands, fp32 accumulators in TMEM).
 //
-// CTA = one (request, 32-token q tile, KV head g).  The 128 MMA rows are the 32 tokens x
-// the 4 query heads that share KV head g (row = 4 * token + head), so every K/V tile is
-// loaded once for the whole GQA group.  Key tiles are 128 keys = 8 blocks of 16: each
-// block's (block, head g) 4 KiB tile is fetched by two 2-D TMA loads (one per 64-dim
+// CTA = one (request, 64-token q tile, KV head g), split into two MMA tiles A and B of
+// 32 tokens each.  The 128 rows of an MMA tile are its 32 tokens x the 4 query heads that
+// share KV head g (row = 4 * token + head), so every K/V tile is loaded once for the
+// whole GQA group and serves both MMA tiles.  Key tiles are 128 keys = 8 blocks of 16:
+// each block's (block, head g) 4 KiB tile is fetched by two 2-D TMA loads (one per 64-dim
 // half, 128-byte swizzle), landing in the canonical K-major SW128 layout.
 //
-// Warp roles (8 warps): warp 0 lane 0 issues TMA loads (Q once, then K/V tiles into a
-// 2-stage ring); warp 1 owns TMEM (512 columns: S double buffer at 0 and 128, O at 256)
-// and lane 0 issues the MMAs; warps 4-7 run the softmax, one thread per MMA row (TMEM
-// lane), and the epilogue.  Per key tile kt:
-//   MMA   : S[kt%2] = Q K_kt^T            (issued one tile ahead)
-//   soft  : m_new = max(m, rowmax S * scale * log2 e); P = 2^(S' - m_new) as bf16;
-//           l = l * 2^(m - m_new) + sum P; once O is stable (previous P V done) rescale O
-//           in TMEM by 2^(m - m_new) when it changed; write P to shared memory
-//           (K-major SW128)
-//   MMA   : O += P V_kt                   (V read MN-major: keys are the K dimension)
-// End: O / l rounded to bf16 and stored for the tile's valid rows.
-// Masking: key position > row position gets -inf (only on tiles that reach past the
-// tile's first row position); V rows at positions >= ctx + q_len in the last tile are
-// zeroed in shared memory so stale bytes cannot leak into P V.
+// Warp roles (12 warps): warp 0 lane 0 issues TMA loads (Q once, then K/V tiles into a
+// 2-stage ring); warp 1 owns TMEM (512 columns: S/P of tile A at 0, of B at 128, O of A
+// at 256, of B at 384) and lane 0 issues the MMAs; warps 4-7 run the softmax of tile A
+// and warps 8-11 that of tile B, one thread per MMA row (TMEM lane).  The MMA warp
+// ping-pongs: O_A += P_A V_kt, S_A = Q_A K_{kt+1}^T, O_B += P_B V_kt, S_B = ..., so the
+// softmax of one tile runs while the tensor core works on the other.  Per key tile a
+// softmax thread: reads its S row from TMEM (pass 1: row max; pass 2: weights),
+// keeps a running max m in base 2 (scores x softmax_scale x log2 e) that moves only when
+// the tile's max exceeds it by more than 8 (then O and l are rescaled in place: until
+// then weights stay below 2^8, which bf16 and fp32 hold exactly enough), writes
+// P = 2^(s - m) as bf16 pairs into TMEM over its S columns, and the P V MMA reads P
+// from TMEM as its A operand (V from shared memory, MN-major: keys are the K dimension).
+// End: O / l rounded to bf16 for the tile's valid rows.
+// Masking: key position > row position gets weight 0 (only on key tiles that reach past
+// the tile's first row position); V rows at positions >= ctx + q_len in the last key
+// tile are zeroed in shared memory so stale bytes cannot leak into P V.
 #include <cuda.h>
 
 #include "kvp_device.cuh"
@@ -36,19 +38,22 @@ namespace kvp {
 
 namespace {
 
-constexpr int kPreThreads = 256;
+constexpr int kPreThreads = 384;
 constexpr int kKeyTile = 128;
 constexpr int kHalfBytes = 16384;   // 128 rows x 128 bytes (64 bf16)
+constexpr int kMmaTokens = kPrefillMmaTokens;   // tokens of one MMA tile (x 4 heads = 128 rows)
+constexpr float kRescaleThreshold = 8.f;
+
+static_assert(kPrefillTileTokens == 2 * kMmaTokens, "a CTA tile is two MMA tiles");
 
 struct __align__(1024) PrefillSmem {
-    uint8_t q[2][kHalfBytes];        // [d half][128 rows]
+    uint8_t q[2][2][kHalfBytes];     // [MMA tile][d half][128 rows]
     uint8_t k[2][2][kHalfBytes];     // [stage][d half][128 keys]
     uint8_t v[2][2][kHalfBytes];     // [stage][d half][128 keys]
-    uint8_t p[2][kHalfBytes];        // [key half][128 rows]
     uint64_t q_full;
     uint64_t k_full[2], v_full[2], kv_empty[2];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_full, o_ready, mma_done;
+    uint64_t s_full[2], p_full[2], o_done[2];   // per MMA tile
+    uint64_t mma_done;
     uint32_t tmem_base;
 };
 
@@ -69,6 +74,135 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+// Softmax and epilogue of one MMA tile (a warpgroup, one thread per row).
+__device__ __forceinline__ void softmax_tile(PrefillSmem& S, const PrefillArgs& a, uint32_t tmem, int t, int wq,
+                                             int lane, int g, int row0, int qpos0, int ntok_t, int nt, int n_kt,
+                                             int n_keys, bool zero_v_rows) {
+    const int row = wq * 32 + lane;
+    const int tl = row >> 2, hl = row & 3;
+    const bool row_valid = tl < ntok_t;
+    const int tq0 = qpos0 + kMmaTokens * t;          // position of the tile's first token
+    const int qpos = row_valid ? tq0 + tl : -1;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t t_s = tmem + t * 128 + lane_off;
+    const uint32_t t_o = tmem + 256 + t * 128 + lane_off;
+    const float sc = a.scale_log2;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int kt = 0; kt < nt; ++kt) {
+        if (!warp_wait(&S.s_full[t], kt & 1)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        const int key0 = kt * kKeyTile;
+        const bool need_mask = key0 + kKeyTile - 1 > tq0;
+        // pass 1: row max of the raw scores over visible keys
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t sr[32];
+            tmem_ld32(t_s + c * 32, sr);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                float f = __uint_as_float(sr[i]);
+                if (need_mask && key0 + c * 32 + i > qpos) f = -INFINITY;
+                mx[i & 3] = fmaxf(mx[i & 3], f);
+            }
+        }
+        const float mx_s = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+        const bool need = mx_s > m_used + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+            const float m_new = fmaxf(m_used, mx_s);
+            const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - m_new);
+            if (kt > 0) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + c * 32, o);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(t_o + c * 32, o);
+                }
+                tc_wait_st();
+            }
+            l *= alpha;
+            m_used = m_new;
+        }
+        const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
+        // pass 2: weights as bf16 pairs into TMEM over the S columns already read
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t sr[32];
+            tmem_ld32(t_s + c * 32, sr);
+            tc_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                float p0 = fast_exp2(fmaf(__uint_as_float(sr[i]), sc, -m_sub));
+                float p1 = fast_exp2(fmaf(__uint_as_float(sr[i + 1]), sc, -m_sub));
+                if (need_mask) {
+                    if (key0 + c * 32 + i > qpos) p0 = 0.f;
+                    if (key0 + c * 32 + i + 1 > qpos) p1 = 0.f;
+                }
+                sum[(i >> 1) & 3] += p0 + p1;
+                pk[i >> 1] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(t_s + c * 16, pk);
+        }
+        tc_wait_st();
+        l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+        if (zero_v_rows && kt == n_kt - 1 && key0 + kKeyTile > n_keys) {
+            // keys at positions >= n_keys hold stale bytes: zero their V rows
+            const int s = kt & 1;
+            if (!warp_wait(&S.v_full[s], (kt >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            if (key0 + row >= n_keys) {
+                const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    *reinterpret_cast<uint4*>(S.v[s][0] + row * 128 + c * 16) = z;
+                    *reinterpret_cast<uint4*>(S.v[s][1] + row * 128 + c * 16) = z;
+                }
+            }
+            fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.p_full[t]);
+    }
+    if (ok && warp_wait(&S.o_done[t], 0)) {
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* orow =
+            a.out + (size_t)(row0 + kMmaTokens * t + tl) * kQRowElems + (g * kGroup + hl) * kHeadDim;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c * 32, o);
+            tc_wait_ld();
+            if (row_valid) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(o[8 * j + 0]) * inv, __uint_as_float(o[8 * j + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(o[8 * j + 2]) * inv, __uint_as_float(o[8 * j + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(o[8 * j + 4]) * inv, __uint_as_float(o[8 * j + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(o[8 * j + 6]) * inv, __uint_as_float(o[8 * j + 7]) * inv);
+                    *reinterpret_cast<uint4*>(orow + c * 32 + j * 8) = w;
+                }
+            }
+        }
+    } else {
+        raise_error(a.err, kErrTimeout);
+    }
+}
+
 __global__ void __launch_bounds__(kPreThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
@@ -85,10 +219,13 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     const int q_len = a.cu[r + 1] - a.cu[r];
     const int row0 = a.cu[r] + tok0;
     const int qpos0 = ctx_r + tok0;
-    const int qpos_last = qpos0 + ntok - 1;
     const int n_keys = ctx_r + q_len;
     const int n_pages = (n_keys + kBlockSize - 1) / kBlockSize;
-    const int n_kt = qpos_last / kKeyTile + 1;
+    const int ntA = min(ntok, kMmaTokens), ntB = max(0, ntok - kMmaTokens);
+    const int nA = (qpos0 + ntA - 1) / kKeyTile + 1;
+    const int nB = ntB > 0 ? (qpos0 + kMmaTokens + ntB - 1) / kKeyTile + 1 : 0;
+    const int n_kt = max(nA, nB);
+    const int zero_tile = (nA == n_kt) ? 0 : 1;   // the first MMA tile that reads the last key tile
 
     if (warp == 1) {
         tmem_alloc(&S.tmem_base, 512);
@@ -101,10 +238,9 @@ __global__ void __launch_bounds__(kPreThreads, 1)
             mbar_init(&S.v_full[s], 1);
             mbar_init(&S.kv_empty[s], 1);
             mbar_init(&S.s_full[s], 1);
-            mbar_init(&S.s_free[s], 4);
+            mbar_init(&S.p_full[s], 4);
+            mbar_init(&S.o_done[s], 1);
         }
-        mbar_init(&S.p_full, 4);
-        mbar_init(&S.o_ready, 1);
         mbar_init(&S.mma_done, 1);
         fence_barrier_init();
     }
@@ -119,9 +255,11 @@ __global__ void __launch_bounds__(kPreThreads, 1)
             prefetch_tmap(&tmap_q);
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
-            mbar_arrive_expect_tx(&S.q_full, 2 * kHalfBytes);
-            tma_load_3d(S.q[0], &tmap_q, 0, g * kGroup, row0, &S.q_full);
-            tma_load_3d(S.q[1], &tmap_q, 64, g * kGroup, row0, &S.q_full);
+            mbar_arrive_expect_tx(&S.q_full, 4 * kHalfBytes);
+            for (int t = 0; t < 2; ++t) {
+                tma_load_3d(S.q[t][0], &tmap_q, 0, g * kGroup, row0 + kMmaTokens * t, &S.q_full);
+                tma_load_3d(S.q[t][1], &tmap_q, 64, g * kGroup, row0 + kMmaTokens * t, &S.q_full);
+            }
             const int32_t* trow = a.tables + (size_t)r * a.max_blocks;
             int issued = 0;
             for (int kt = 0; kt < n_kt; ++kt) {
@@ -167,42 +305,53 @@ __global__ void __launch_bounds__(kPreThreads, 1)
             // ------------------------------------------------------------ MMA issuer
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, 1);
-            const uint32_t sq = smem_u32(S.q[0]), sp = smem_u32(S.p[0]);
             bool ok = mbar_wait(&S.q_full, 0);
-            auto issue_qk = [&](int j) -> bool {
-                const int s = j & 1;
-                if (!mbar_wait(&S.k_full[s], (j >> 1) & 1)) return false;
-                if (j >= 2 && !mbar_wait(&S.s_free[s], ((j >> 1) - 1) & 1)) return false;
+            auto issue_qk = [&](int t, int kt) -> bool {
+                const int s = kt & 1;
+                if (!mbar_wait(&S.k_full[s], (kt >> 1) & 1)) return false;
                 tc_fence_after();
-                const uint32_t sk = smem_u32(S.k[s][0]);
+                const uint32_t sq = smem_u32(S.q[t][0]), sk = smem_u32(S.k[s][0]);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    tc_mma_f16(tmem + s * 128, smem_desc_sw128(sq + koff, 16, 1024),
+                    tc_mma_f16(tmem + t * 128, smem_desc_sw128(sq + koff, 16, 1024),
                                smem_desc_sw128(sk + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(&S.s_full[s]);
+                tc_commit(&S.s_full[t]);
                 return true;
             };
-            if (ok) ok = issue_qk(0);
-            for (int kt = 0; kt < n_kt && ok; ++kt) {
-                if (kt + 1 < n_kt && !(ok = issue_qk(kt + 1))) break;
+            auto issue_pv = [&](int t, int kt) -> bool {
                 const int s = kt & 1;
-                if (!mbar_wait(&S.p_full, kt & 1) || !mbar_wait(&S.v_full[s], (kt >> 1) & 1)) {
-                    ok = false;
-                    break;
-                }
+                if (!mbar_wait(&S.p_full[t], kt & 1) || !mbar_wait(&S.v_full[s], (kt >> 1) & 1)) return false;
                 tc_fence_after();
                 const uint32_t sv = smem_u32(S.v[s][0]);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t poff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    tc_mma_f16(tmem + 256, smem_desc_sw128(sp + poff, 16, 1024),
-                               smem_desc_sw128(sv + kk * 2048, kHalfBytes, 1024), idesc_pv,
-                               (kt > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma_f16_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                                  smem_desc_sw128(sv + kk * 2048, kHalfBytes, 1024), idesc_pv,
+                                  (kt > 0 || kk > 0) ? 1u : 0u);
+                return true;
+            };
+            if (ok && nA > 0) ok = issue_qk(0, 0);
+            if (ok && nB > 0) ok = issue_qk(1, 0);
+            for (int kt = 0; kt < n_kt && ok; ++kt) {
+                if (kt < nA) {
+                    if (!(ok = issue_pv(0, kt))) break;
+                    if (kt + 1 < nA) {
+                        if (!(ok = issue_qk(0, kt + 1))) break;
+                    } else {
+                        tc_commit(&S.o_done[0]);
+                    }
                 }
-                tc_commit(&S.o_ready);
-                tc_commit(&S.kv_empty[s]);
+                if (kt < nB) {
+                    if (!(ok = issue_pv(1, kt))) break;
+                    if (kt + 1 < nB) {
+                        if (!(ok = issue_qk(1, kt + 1))) break;
+                    } else {
+                        tc_commit(&S.o_done[1]);
+                    }
+                }
+                tc_commit(&S.kv_empty[kt & 1]);
             }
             if (!ok) raise_error(a.err, kErrTimeout);
             // No MMA may still be running when TMEM is released.
@@ -211,129 +360,11 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         }
     } else if (warp >= 4) {
         // --------------------------------------------------------- softmax + epilogue
-        const int wq = warp - 4;
-        const int row = wq * 32 + lane;
-        const int tl = row >> 2, hl = row & 3;
-        const bool row_valid = tl < ntok;
-        const int qpos = row_valid ? qpos0 + tl : -1;
-        const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
-        float m = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int kt = 0; kt < n_kt; ++kt) {
-            const int s = kt & 1;
-            if (!warp_wait(&S.s_full[s], (kt >> 1) & 1)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tmem_ld32(t_lane + s * 128 + cc * 32, sr[cc]);
-            tc_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.s_free[s]);
-
-            const int key0 = kt * kKeyTile;
-            const bool need_mask = key0 + kKeyTile - 1 > qpos0;
-            float mx = -INFINITY;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float f = __uint_as_float(sr[cc][i]) * a.scale_log2;
-                    if (need_mask && key0 + cc * 32 + i > qpos) f = -INFINITY;
-                    sr[cc][i] = __float_as_uint(f);
-                    mx = fmaxf(mx, f);
-                }
-            const float m_new = fmaxf(m, mx);
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = fast_exp2(m - m_use);
-            float sum = 0.f;
-            uint32_t pk[64];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const float p0 = fast_exp2(__uint_as_float(sr[cc][i]) - m_use);
-                    const float p1 = fast_exp2(__uint_as_float(sr[cc][i + 1]) - m_use);
-                    sum += p0 + p1;
-                    pk[cc * 16 + i / 2] = pack_bf16x2(p0, p1);
-                }
-            l = l * alpha + sum;
-            m = m_new;
-
-            if (kt > 0) {
-                // O is stable once the previous P V has completed; P's buffer is free too.
-                if (!warp_wait(&S.o_ready, (kt - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        uint32_t o[32];
-                        tmem_ld32(t_lane + 256 + cc * 32, o);
-                        tc_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(t_lane + 256 + cc * 32, o);
-                    }
-                    tc_wait_st();
-                }
-            }
-            if (kt == n_kt - 1 && key0 + kKeyTile > n_keys) {
-                // keys at positions >= n_keys hold stale bytes: zero their V rows
-                if (!warp_wait(&S.v_full[s], (kt >> 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                if (key0 + row >= n_keys) {
-                    const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        *reinterpret_cast<uint4*>(S.v[s][0] + row * 128 + c * 16) = z;
-                        *reinterpret_cast<uint4*>(S.v[s][1] + row * 128 + c * 16) = z;
-                    }
-                }
-            }
-            // P row -> shared memory, K-major with 128-byte swizzle (16-byte chunk c of
-            // row r sits at chunk position c ^ (r % 8) within the row's 128 bytes).
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint4 w = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                *reinterpret_cast<uint4*>(S.p[c >> 3] + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = w;
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.p_full);
-        }
-        if (ok && warp_wait(&S.o_ready, (n_kt - 1) & 1)) {
-            tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16* orow = a.out + (size_t)(row0 + tl) * kQRowElems + (g * kGroup + hl) * kHeadDim;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t o[32];
-                tmem_ld32(t_lane + 256 + cc * 32, o);
-                tc_wait_ld();
-                if (row_valid) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + cc * 32 + c * 8) = w;
-                    }
-                }
-            }
-        } else {
-            raise_error(a.err, kErrTimeout);
-        }
+        const int t = (warp - 4) >> 2;
+        const int nt = t ? nB : nA;
+        if (nt > 0)
+            softmax_tile(S, a, tmem, t, warp & 3, lane, g, row0, qpos0, t ? ntB : ntA, nt, n_kt, n_keys,
+                         t == zero_tile);
     }
     tc_fence_before();
     __syncthreads();

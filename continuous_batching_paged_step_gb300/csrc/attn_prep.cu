@@ -8,8 +8,9 @@
 //     page_off[r] is the exclusive prefix sum of those block counts over the requests
 //     (0 blocks for other requests), page_off[num_reqs] the total.  The decode kernel
 //     shares the total out evenly among its CTAs.
-//   q_r >= 2 (prefill chunk): one tile per 32 query tokens (x 4 query heads of a KV group
-//     = 128 MMA rows), emitted last tile first so the longest tiles start earliest.
+//   q_r >= 2 (prefill chunk): one tile per 64 query tokens (two MMA tiles of 32 tokens x
+//     4 query heads of a KV group), emitted last tile first so the longest tiles start
+//     earliest.
 // One CTA of 1024 threads scans the requests in rounds of 1024 (block-wide exclusive
 // scan).  Inconsistent metadata sets KVP_ERRBIT_BAD_META; a request that fails its own
 // checks gets no work, and a cu_seqlens array that is not a monotone map of

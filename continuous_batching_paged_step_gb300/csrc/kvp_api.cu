@@ -93,7 +93,7 @@ bool encode_q_map(CUtensorMap* m, const void* q, int num_tokens) {
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)kvp::kHeadDim, (cuuint64_t)kvp::kNumQHeads, (cuuint64_t)num_tokens};
     const cuuint64_t strides[2] = {(cuuint64_t)kvp::kHeadBytes, (cuuint64_t)kvp::kQRowElems * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kvp::kGroup, (cuuint32_t)kvp::kPrefillTileTokens};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kvp::kGroup, (cuuint32_t)kvp::kPrefillMmaTokens};
     const cuuint32_t es[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,

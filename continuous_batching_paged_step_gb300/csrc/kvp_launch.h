@@ -62,7 +62,9 @@ cudaError_t launch_prefill(const StepArgs& a, const CUtensorMap* tmap_q, const C
 // One-time per-device kernel attributes (dynamic shared memory limits).
 cudaError_t configure_kernels();
 
-// Tokens per prefill q tile (x 4 query heads of one KV group = 128 MMA rows).
-constexpr int kPrefillTileTokens = 32;
+// Prefill work unit: a CTA takes 64 query tokens of one request and one KV group, as two
+// MMA tiles of 32 tokens x 4 query heads = 128 rows each.
+constexpr int kPrefillTileTokens = 64;
+constexpr int kPrefillMmaTokens = 32;
 
 }  // namespace kvp
