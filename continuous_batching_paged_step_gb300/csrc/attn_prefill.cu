@@ -98,20 +98,25 @@ __device__ __forceinline__ void softmax_tile(PrefillSmem& S, const PrefillArgs& 
         const int key0 = kt * kKeyTile;
         const bool need_mask = key0 + kKeyTile - 1 > tq0;
         // pass 1: row max of the raw scores over visible keys
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             uint32_t sr[32];
             tmem_ld32(t_s + c * 32, sr);
             tc_wait_ld();
+            if (need_mask) {
+                const int lim = qpos - key0 - c * 32;   // column i is visible iff i <= lim
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                float f = __uint_as_float(sr[i]);
-                if (need_mask && key0 + c * 32 + i > qpos) f = -INFINITY;
-                mx[i & 3] = fmaxf(mx[i & 3], f);
+                for (int i = 0; i < 32; ++i)
+                    if (i > lim) sr[i] = __float_as_uint(-INFINITY);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                mx[0] = fmax3(mx[0], __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+                mx[1] = fmax3(mx[1], __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
             }
         }
-        const float mx_s = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+        const float mx_s = fmaxf(mx[0], mx[1]) * sc;
         const bool need = mx_s > m_used + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
             const float m_new = fmaxf(m_used, mx_s);
@@ -133,28 +138,31 @@ __device__ __forceinline__ void softmax_tile(PrefillSmem& S, const PrefillArgs& 
         }
         const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
         // pass 2: weights as bf16 pairs into TMEM over the S columns already read
-        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+        const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_sub, -m_sub);
+        float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             uint32_t sr[32];
             tmem_ld32(t_s + c * 32, sr);
             tc_wait_ld();
+            if (need_mask) {
+                const int lim = qpos - key0 - c * 32;   // keys after the row's position get weight 0
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (i > lim) sr[i] = __float_as_uint(-INFINITY);
+            }
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-                float p0 = fast_exp2(fmaf(__uint_as_float(sr[i]), sc, -m_sub));
-                float p1 = fast_exp2(fmaf(__uint_as_float(sr[i + 1]), sc, -m_sub));
-                if (need_mask) {
-                    if (key0 + c * 32 + i > qpos) p0 = 0.f;
-                    if (key0 + c * 32 + i + 1 > qpos) p1 = 0.f;
-                }
-                sum[(i >> 1) & 3] += p0 + p1;
-                pk[i >> 1] = pack_bf16x2(p0, p1);
+                const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sc2, nm2);
+                const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                sum2[(i >> 1) & 1] = __fadd2_rn(sum2[(i >> 1) & 1], p);
+                pk[i >> 1] = pack_bf16x2(p.x, p.y);
             }
             tmem_st16(t_s + c * 16, pk);
         }
         tc_wait_st();
-        l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+        l += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
         if (zero_v_rows && kt == n_kt - 1 && key0 + kKeyTile > n_keys) {
             // keys at positions >= n_keys hold stale bytes: zero their V rows
             const int s = kt & 1;
