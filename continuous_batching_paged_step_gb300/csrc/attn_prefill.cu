@@ -13,13 +13,13 @@
 // each block's (block, head g) 4 KiB tile is fetched by two 2-D TMA loads (one per 64-dim
 // half, 128-byte swizzle), landing in the canonical K-major SW128 layout.
 //
-// Warp roles (12 warps): warp 0 lane 0 issues TMA loads (Q once, then K/V tiles into a
-// 2-stage ring); warp 1 owns TMEM (512 columns: S/P of tile A at 0, of B at 128, O of A
+// Warp roles (12 warps): warp 0 lane 0 issues the TMA loads of Q (once) and of K tiles
+// into a 3-stage ring, warp 2 lane 0 those of V tiles into a 2-stage ring; warp 1 owns TMEM (512 columns: S/P of tile A at 0, of B at 128, O of A
 // at 256, of B at 384) and lane 0 issues the MMAs; warps 4-7 run the softmax of tile A
 // and warps 8-11 that of tile B, one thread per MMA row (TMEM lane).  The MMA warp
 // ping-pongs: O_A += P_A V_kt, S_A = Q_A K_{kt+1}^T, O_B += P_B V_kt, S_B = ..., so the
 // softmax of one tile runs while the tensor core works on the other.  Per key tile a
-// softmax thread: reads its S row from TMEM (pass 1: row max; pass 2: weights),
+// softmax thread: reads its whole S row from TMEM in one load,
 // keeps a running max m in base 2 (scores x softmax_scale x log2 e) that moves only when
 // the tile's max exceeds it by more than 8 (then O and l are rescaled in place: until
 // then weights stay below 2^8, which bf16 and fp32 hold exactly enough), writes
@@ -43,15 +43,20 @@ constexpr int kKeyTile = 128;
 constexpr int kHalfBytes = 16384;   // 128 rows x 128 bytes (64 bf16)
 constexpr int kMmaTokens = kPrefillMmaTokens;   // tokens of one MMA tile (x 4 heads = 128 rows)
 constexpr float kRescaleThreshold = 8.f;
+// K is needed one softmax earlier than V, so its ring is deeper: 3 K + 2 V stages of
+// 32 KiB, with Q (64 KiB) 224 KiB of shared memory.
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
 
 static_assert(kPrefillTileTokens == 2 * kMmaTokens, "a CTA tile is two MMA tiles");
 
 struct __align__(1024) PrefillSmem {
     uint8_t q[2][2][kHalfBytes];     // [MMA tile][d half][128 rows]
-    uint8_t k[2][2][kHalfBytes];     // [stage][d half][128 keys]
-    uint8_t v[2][2][kHalfBytes];     // [stage][d half][128 keys]
+    uint8_t k[kKStages][2][kHalfBytes];   // [stage][d half][128 keys]
+    uint8_t v[kVStages][2][kHalfBytes];   // [stage][d half][128 keys]
     uint64_t q_full;
-    uint64_t k_full[2], v_full[2], kv_empty[2];
+    uint64_t k_full[kKStages], k_empty[kKStages];
+    uint64_t v_full[kVStages], v_empty[kVStages];
     uint64_t s_full[2], p_full[2], o_done[2];   // per MMA tile
     uint64_t mma_done;
     uint32_t tmem_base;
@@ -97,26 +102,25 @@ __device__ __forceinline__ void softmax_tile(PrefillSmem& S, const PrefillArgs& 
         tc_fence_after();
         const int key0 = kt * kKeyTile;
         const bool need_mask = key0 + kKeyTile - 1 > tq0;
-        // pass 1: row max of the raw scores over visible keys
-        float mx[2] = {-INFINITY, -INFINITY};
+        // the whole S row in one TMEM load
+        uint32_t sr[128];
+        tmem_ld128(t_s, sr);
+        tc_wait_ld();
+        if (need_mask) {
+            const int lim = qpos - key0;   // column i is visible iff i <= lim
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t sr[32];
-            tmem_ld32(t_s + c * 32, sr);
-            tc_wait_ld();
-            if (need_mask) {
-                const int lim = qpos - key0 - c * 32;   // column i is visible iff i <= lim
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i > lim) sr[i] = __float_as_uint(-INFINITY);
-            }
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-                mx[0] = fmax3(mx[0], __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
-                mx[1] = fmax3(mx[1], __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
-            }
+            for (int i = 0; i < 128; ++i)
+                if (i > lim) sr[i] = __float_as_uint(-INFINITY);
         }
-        const float mx_s = fmaxf(mx[0], mx[1]) * sc;
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < 128; i += 8) {
+            mx[0] = fmax3(mx[0], __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+            mx[1] = fmax3(mx[1], __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+            mx[2] = fmax3(mx[2], __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
+            mx[3] = fmax3(mx[3], __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
+        }
+        const float mx_s = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
         const bool need = mx_s > m_used + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
             const float m_new = fmaxf(m_used, mx_s);
@@ -137,36 +141,24 @@ __device__ __forceinline__ void softmax_tile(PrefillSmem& S, const PrefillArgs& 
             m_used = m_new;
         }
         const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
-        // pass 2: weights as bf16 pairs into TMEM over the S columns already read
+        // weights 2^(s * scale - m) as bf16 pairs, packed in place (pair j -> sr[j]), then
+        // written over the S columns in one TMEM store
         const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_sub, -m_sub);
         float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t sr[32];
-            tmem_ld32(t_s + c * 32, sr);
-            tc_wait_ld();
-            if (need_mask) {
-                const int lim = qpos - key0 - c * 32;   // keys after the row's position get weight 0
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i > lim) sr[i] = __float_as_uint(-INFINITY);
-            }
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sc2, nm2);
-                const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-                sum2[(i >> 1) & 1] = __fadd2_rn(sum2[(i >> 1) & 1], p);
-                pk[i >> 1] = pack_bf16x2(p.x, p.y);
-            }
-            tmem_st16(t_s + c * 16, pk);
+        for (int i = 0; i < 128; i += 2) {
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sc2, nm2);
+            const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            sum2[(i >> 1) & 1] = __fadd2_rn(sum2[(i >> 1) & 1], p);
+            sr[i >> 1] = pack_bf16x2(p.x, p.y);
         }
+        tmem_st64(t_s, sr);
         tc_wait_st();
         l += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
         if (zero_v_rows && kt == n_kt - 1 && key0 + kKeyTile > n_keys) {
             // keys at positions >= n_keys hold stale bytes: zero their V rows
-            const int s = kt & 1;
-            if (!warp_wait(&S.v_full[s], (kt >> 1) & 1)) {
+            const int s = kt % kVStages;
+            if (!warp_wait(&S.v_full[s], (kt / kVStages) & 1)) {
                 ok = false;
                 break;
             }
@@ -241,10 +233,15 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     }
     if (threadIdx.x == 0) {
         mbar_init(&S.q_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(&S.k_full[s], 1);
+            mbar_init(&S.k_empty[s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
             mbar_init(&S.v_full[s], 1);
-            mbar_init(&S.kv_empty[s], 1);
+            mbar_init(&S.v_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(&S.s_full[s], 1);
             mbar_init(&S.p_full[s], 4);
             mbar_init(&S.o_done[s], 1);
@@ -257,56 +254,66 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     tc_fence_after();
     const uint32_t tmem = S.tmem_base;
 
-    if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------------------ TMA producer
+    if ((warp == 0 || warp == 2) && lane == 0) {
+        // ---------------------------------------------- TMA producers: K (warp 0), V (warp 2)
+        const bool is_k = warp == 0;
+        const CUtensorMap* tm = is_k ? &tmap_k : &tmap_v;
+        const int nst = is_k ? kKStages : kVStages;
+        prefetch_tmap(tm);
+        if (is_k) {
             prefetch_tmap(&tmap_q);
-            prefetch_tmap(&tmap_k);
-            prefetch_tmap(&tmap_v);
             mbar_arrive_expect_tx(&S.q_full, 4 * kHalfBytes);
             for (int t = 0; t < 2; ++t) {
                 tma_load_3d(S.q[t][0], &tmap_q, 0, g * kGroup, row0 + kMmaTokens * t, &S.q_full);
                 tma_load_3d(S.q[t][1], &tmap_q, 64, g * kGroup, row0 + kMmaTokens * t, &S.q_full);
             }
-            const int32_t* trow = a.tables + (size_t)r * a.max_blocks;
-            int issued = 0;
-            for (int kt = 0; kt < n_kt; ++kt) {
-                const int s = kt & 1;
-                if (!mbar_wait(&S.kv_empty[s], ((kt >> 1) & 1) ^ 1)) {
-                    raise_error(a.err, kErrTimeout);
-                    break;
-                }
-                const int pg0 = kt * (kKeyTile / kBlockSize);
-                const int npg = min(kKeyTile / kBlockSize, n_pages - pg0);
-                int rows[kKeyTile / kBlockSize];
+        }
+        const int32_t* trow = a.tables + (size_t)r * a.max_blocks;
+        constexpr int kPages = kKeyTile / kBlockSize;
+        // block-table entries of key tile kt, read one tile ahead so their latency
+        // overlaps the wait for a free stage
+        int next[kPages];
+        auto read_rows = [&](int kt, int (&dst)[kPages]) {
+            const int pg0 = kt * kPages;
 #pragma unroll
-                for (int j = 0; j < kKeyTile / kBlockSize; ++j) {
-                    int b = j < npg ? trow[pg0 + j] : 0;
-                    if ((unsigned)b >= (unsigned)a.num_blocks) {
-                        raise_error(a.err, kErrBadBlock);
-                        b = 0;
-                    }
-                    rows[j] = (b * kNumKvHeads + g) * kBlockSize;
+            for (int j = 0; j < kPages; ++j) dst[j] = (kt < n_kt && pg0 + j < n_pages) ? trow[pg0 + j] : 0;
+        };
+        read_rows(0, next);
+        int issued = 0;
+        for (int kt = 0; kt < n_kt; ++kt) {
+            const int s = kt % nst;
+            const uint32_t ph = (kt / nst) & 1;
+            int rows[kPages];
+#pragma unroll
+            for (int j = 0; j < kPages; ++j) {
+                int b = next[j];
+                if ((unsigned)b >= (unsigned)a.num_blocks) {
+                    if (is_k) raise_error(a.err, kErrBadBlock);
+                    b = 0;
                 }
-                mbar_arrive_expect_tx(&S.k_full[s], npg * kTileBytes);
-                for (int j = 0; j < npg; ++j) {
-                    tma_load_2d(S.k[s][0] + j * 2048, &tmap_k, 0, rows[j], &S.k_full[s]);
-                    tma_load_2d(S.k[s][1] + j * 2048, &tmap_k, 64, rows[j], &S.k_full[s]);
-                }
-                mbar_arrive_expect_tx(&S.v_full[s], npg * kTileBytes);
-                for (int j = 0; j < npg; ++j) {
-                    tma_load_2d(S.v[s][0] + j * 2048, &tmap_v, 0, rows[j], &S.v_full[s]);
-                    tma_load_2d(S.v[s][1] + j * 2048, &tmap_v, 64, rows[j], &S.v_full[s]);
-                }
-                ++issued;
+                rows[j] = (b * kNumKvHeads + g) * kBlockSize;
             }
-            // Drain: wait until every copy issued into this CTA's shared memory landed.
-            if (!mbar_wait(&S.q_full, 0)) raise_error(a.err, kErrTimeout);
-            for (int kt = issued - 2 < 0 ? 0 : issued - 2; kt < issued; ++kt) {
-                const int s = kt & 1;
-                const uint32_t ph = (kt >> 1) & 1;
-                if (!mbar_wait(&S.k_full[s], ph) || !mbar_wait(&S.v_full[s], ph)) raise_error(a.err, kErrTimeout);
+            read_rows(kt + 1, next);
+            uint64_t* empty = is_k ? &S.k_empty[s] : &S.v_empty[s];
+            uint64_t* full = is_k ? &S.k_full[s] : &S.v_full[s];
+            uint8_t* dst = is_k ? S.k[s][0] : S.v[s][0];
+            if (!mbar_wait(empty, ph ^ 1)) {
+                raise_error(a.err, kErrTimeout);
+                break;
             }
+            const int npg = min(kPages, n_pages - kt * kPages);
+            mbar_arrive_expect_tx(full, npg * kTileBytes);
+            for (int j = 0; j < npg; ++j) {
+                tma_load_2d(dst + j * 2048, tm, 0, rows[j], full);
+                tma_load_2d(dst + kHalfBytes + j * 2048, tm, 64, rows[j], full);
+            }
+            ++issued;
+        }
+        // Drain: wait until every copy issued into this CTA's shared memory landed.
+        if (is_k && !mbar_wait(&S.q_full, 0)) raise_error(a.err, kErrTimeout);
+        for (int kt = issued - nst < 0 ? 0 : issued - nst; kt < issued; ++kt) {
+            uint64_t* full = is_k ? &S.k_full[kt % nst] : &S.v_full[kt % nst];
+            if (!mbar_wait(full, (kt / nst) & 1)) raise_error(a.err, kErrTimeout);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -315,8 +322,8 @@ __global__ void __launch_bounds__(kPreThreads, 1)
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, 1);
             bool ok = mbar_wait(&S.q_full, 0);
             auto issue_qk = [&](int t, int kt) -> bool {
-                const int s = kt & 1;
-                if (!mbar_wait(&S.k_full[s], (kt >> 1) & 1)) return false;
+                const int s = kt % kKStages;
+                if (!mbar_wait(&S.k_full[s], (kt / kKStages) & 1)) return false;
                 tc_fence_after();
                 const uint32_t sq = smem_u32(S.q[t][0]), sk = smem_u32(S.k[s][0]);
 #pragma unroll
@@ -326,11 +333,12 @@ __global__ void __launch_bounds__(kPreThreads, 1)
                                smem_desc_sw128(sk + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&S.s_full[t]);
+                if (t == 1 || kt >= nB) tc_commit(&S.k_empty[s]);   // last QK that reads this K stage
                 return true;
             };
             auto issue_pv = [&](int t, int kt) -> bool {
-                const int s = kt & 1;
-                if (!mbar_wait(&S.p_full[t], kt & 1) || !mbar_wait(&S.v_full[s], (kt >> 1) & 1)) return false;
+                const int s = kt % kVStages;
+                if (!mbar_wait(&S.p_full[t], kt & 1) || !mbar_wait(&S.v_full[s], (kt / kVStages) & 1)) return false;
                 tc_fence_after();
                 const uint32_t sv = smem_u32(S.v[s][0]);
 #pragma unroll
@@ -338,6 +346,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
                     tc_mma_f16_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
                                   smem_desc_sw128(sv + kk * 2048, kHalfBytes, 1024), idesc_pv,
                                   (kt > 0 || kk > 0) ? 1u : 0u);
+                if (t == 1 || kt >= nB) tc_commit(&S.v_empty[s]);   // last P V that reads this V stage
                 return true;
             };
             if (ok && nA > 0) ok = issue_qk(0, 0);
@@ -359,7 +368,6 @@ __global__ void __launch_bounds__(kPreThreads, 1)
                         tc_commit(&S.o_done[1]);
                     }
                 }
-                tc_commit(&S.kv_empty[kt & 1]);
             }
             if (!ok) raise_error(a.err, kErrTimeout);
             // No MMA may still be running when TMEM is released.

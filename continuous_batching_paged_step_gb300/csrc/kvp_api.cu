@@ -9,7 +9,7 @@
 #include <new>
 #include <vector>
 
-#include "../../include/kvpaged.h"
+#include "kvpaged.h"
 #include "kvp_device.cuh"
 #include "kvp_launch.h"
 
