@@ -451,6 +451,15 @@ kvp_status kv_pool_read_timing(kvp_pool* p, int* counts, float* ms) {
 
 long long kv_pool_launch_count(const kvp_pool* p) { return p ? p->launches : -1; }
 
+}  // extern "C"
+
+namespace kvp {
+// Device the pool's device-side state lives on, or -1 if it has none yet.
+int pool_device(const kvp_pool* p) { return p ? p->device : -1; }
+}  // namespace kvp
+
+extern "C" {
+
 const char* kvp_status_string(kvp_status s) {
     switch (s) {
         case KVP_OK: return "ok";

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+struct kvp_pool;
+
 namespace kvp {
 
 // Scratch layout inside the caller's workspace for one paged_attention_step call.
@@ -58,6 +60,9 @@ cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const StepArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
                            const CUtensorMap* tmap_v, cudaStream_t stream);
+
+// Device the pool's device-side state lives on, or -1 if it has none yet.
+int pool_device(const ::kvp_pool* p);
 
 // One-time per-device kernel attributes (dynamic shared memory limits).
 cudaError_t configure_kernels();

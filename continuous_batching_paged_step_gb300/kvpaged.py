@@ -42,6 +42,8 @@ SIGNATURES = {
     "kv_pool_enable_timing": (_I, [_P, _I]),
     "kv_pool_read_timing": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_F)]),
     "kv_pool_launch_count": (ctypes.c_longlong, [_P]),
+    "paged_attention_step_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "paged_attention_noalloc_capacity": (_SZ, []),
 }
 KERNEL_NAMES = ("kv_append", "step_prep", "prefill_tcgen05", "decode_splitkv", "splitkv_combine")
 
@@ -239,3 +241,25 @@ class KVPool:
             self.close()
         except Exception:
             pass
+
+
+def paged_attention_step_noalloc(pool: int, q, out, cu_seqlens_q, context_lens, block_tables, max_q_len: int,
+                                 max_context_len: int, softmax_scale: float, stream=None):
+    """paged_attention_step without a caller workspace: the library's fixed scratch array
+    is used instead, so the call allocates no device memory (see include/kvpaged.h)."""
+    import torch
+    T = q.shape[0]
+    if T:
+        _need(q, torch.bfloat16, "q")
+        _need(out, torch.bfloat16, "out")
+        for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (context_lens, "context_lens"), (block_tables, "block_tables")):
+            _need(t, torch.int32, n)
+    R = context_lens.shape[0]
+    _check(lib.paged_attention_step_noalloc(pool, _ptr(q), _ptr(out), _ptr(cu_seqlens_q), _ptr(context_lens),
+                                            _ptr(block_tables), block_tables.shape[1], R, T, N_Q_HEADS, max_q_len,
+                                            max_context_len, float(softmax_scale), _stream(stream)),
+           "paged_attention_step_noalloc")
+
+
+def paged_attention_noalloc_capacity() -> int:
+    return lib.paged_attention_noalloc_capacity()

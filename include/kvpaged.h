@@ -194,6 +194,32 @@ KVP_API kvp_status kv_pool_set_decode_ctas(kvp_pool* pool, int ctas);
  * else the status of the lowest set bit (BAD_BLOCK, SHARED_WRITE, BAD_META, TIMEOUT). */
 KVP_API kvp_status kv_pool_get_error(kvp_pool* pool, kvp_stream stream, uint32_t* bits);
 
+/* ---------------------------------------------------------- allocation-free step ----
+ * The pages have no counterpart: this is a convenience of this library.
+ * Same as paged_attention_step, but without a caller workspace: for callers that cannot
+ * allocate device memory at step time (an engine that gave all free device memory to
+ * its KV pool, or a serving loop that must not call cudaMalloc/cudaFree because they can
+ * synchronise the device).  The scratch lives in a fixed device array inside the library
+ * (paged_attention_noalloc_capacity() bytes, 32 MiB), held by every GPU that loads the
+ * library until the process exits.  The call allocates nothing: the pool must already
+ * have its device state (made by its first kv_append on the current device), else
+ * KVP_E_INVALID_ARG.  A step whose scratch (paged_attention_workspace_size) exceeds the
+ * array is rejected with KVP_E_WORKSPACE before anything is launched.  All calls share
+ * the array: calls whose kernels overlap on the GPU (other streams, other threads) race
+ * on it; calls on one stream are ordered.  Nothing in it needs to start at zero.  The
+ * first call with a given device current looks the array's device address up
+ * (cudaGetSymbolAddress); make it before any stream capture begins. */
+KVP_API kvp_status paged_attention_step_noalloc(kvp_pool* pool, const void* q, void* out,
+                                                const int32_t* cu_seqlens_q,
+                                                const int32_t* context_lens,
+                                                const int32_t* block_tables, int max_blocks_per_seq,
+                                                int num_reqs, int num_tokens, int n_q_heads,
+                                                int max_q_len, int max_context_len,
+                                                float softmax_scale, kvp_stream stream);
+
+/* Bytes of the fixed scratch array used by paged_attention_step_noalloc. */
+KVP_API size_t paged_attention_noalloc_capacity(void);
+
 /* ------------------------------------------------------------------ diagnostics ----
  * Per-kernel timing of the library's own launches, for benchmarks.  After
  * kv_pool_enable_timing(pool, max_launches) every kernel launch of kv_append and
