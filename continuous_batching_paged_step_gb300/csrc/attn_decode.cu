@@ -158,6 +158,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
     extern __shared__ uint8_t smem_raw[];
     DecodeSmem& S = *reinterpret_cast<DecodeSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    grid_dep_wait();     // block offsets, cache contents
+    grid_dep_launch();
     const int P = page_off[num_reqs];
     int lo, hi;
     cta_range(P, blockIdx.x, gridDim.x, lo, hi);
@@ -386,6 +388,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict_
                                                       const float2* __restrict__ part_ml,
                                                       __nv_bfloat16* __restrict__ out) {
     const int r = blockIdx.x;
+    grid_dep_wait();     // partials of the decode kernel
     const int P = page_off[num_reqs];
     const int a = page_off[r], b = page_off[r + 1];
     if (b <= a) return;
@@ -427,24 +430,22 @@ int decode_grid(const StepArgs& a) {
 cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream) {
     const StepLayout& L = a.lay;
     const size_t smem = sizeof(DecodeSmem) + 128;
-    decode_kernel<<<decode_grid(a), kDecThreads, smem, stream>>>(
-        static_cast<const __nv_bfloat16*>(a.q), static_cast<__nv_bfloat16*>(a.out), a.cu_seqlens_q, a.context_lens,
-        a.block_tables, a.max_blocks_per_seq, a.num_blocks, static_cast<const uint8_t*>(a.k_cache),
-        static_cast<const uint8_t*>(a.v_cache), reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs,
-        reinterpret_cast<float*>(a.ws + L.part_acc_off), reinterpret_cast<float2*>(a.ws + L.part_ml_off),
-        a.softmax_scale * 1.4426950408889634f, a.err);
-    return cudaGetLastError();
+    return launch_pdl(decode_kernel, dim3(decode_grid(a)), dim3(kDecThreads), smem, stream,
+                      static_cast<const __nv_bfloat16*>(a.q), static_cast<__nv_bfloat16*>(a.out), a.cu_seqlens_q,
+                      a.context_lens, a.block_tables, a.max_blocks_per_seq, a.num_blocks,
+                      static_cast<const uint8_t*>(a.k_cache), static_cast<const uint8_t*>(a.v_cache),
+                      reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs,
+                      reinterpret_cast<float*>(a.ws + L.part_acc_off), reinterpret_cast<float2*>(a.ws + L.part_ml_off),
+                      a.softmax_scale * 1.4426950408889634f, a.err);
 }
 
 cudaError_t launch_combine(const StepArgs& a, cudaStream_t stream) {
     const StepLayout& L = a.lay;
     dim3 grid(a.num_reqs, kNumQHeads / 8);
-    combine_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs,
-                                             decode_grid(a), a.cu_seqlens_q,
-                                             reinterpret_cast<const float*>(a.ws + L.part_acc_off),
-                                             reinterpret_cast<const float2*>(a.ws + L.part_ml_off),
-                                             static_cast<__nv_bfloat16*>(a.out));
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, grid, dim3(256), 0, stream,
+                      reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs, decode_grid(a),
+                      a.cu_seqlens_q, reinterpret_cast<const float*>(a.ws + L.part_acc_off),
+                      reinterpret_cast<const float2*>(a.ws + L.part_ml_off), static_cast<__nv_bfloat16*>(a.out));
 }
 
 cudaError_t configure_decode_kernel() {

@@ -210,6 +210,8 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     PrefillSmem& S =
         *reinterpret_cast<PrefillSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tile = blockIdx.x, g = blockIdx.y;
+    grid_dep_wait();     // work list, cache contents
+    grid_dep_launch();
     if (tile >= a.counters[1]) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -409,8 +411,7 @@ cudaError_t launch_prefill(const StepArgs& a, const CUtensorMap* tmap_q, const C
     pa.scale_log2 = a.softmax_scale * 1.4426950408889634f;
     dim3 grid(L.max_prefill_tiles, kNumKvHeads);
     const size_t smem = sizeof(PrefillSmem) + 1024;
-    prefill_kernel<<<grid, kPreThreads, smem, stream>>>(*tmap_q, *tmap_k, *tmap_v, pa);
-    return cudaGetLastError();
+    return launch_pdl(prefill_kernel, grid, dim3(kPreThreads), smem, stream, *tmap_q, *tmap_k, *tmap_v, pa);
 }
 
 cudaError_t configure_prefill_kernel() {

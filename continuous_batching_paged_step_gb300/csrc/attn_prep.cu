@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(kPrepThreads) step_prep_kernel(
     __shared__ int2 s_warp[32];
     __shared__ int2 s_base;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    grid_dep_launch();
     if (tid == 0) {
         s_ok = (cu[0] == 0 && cu[num_reqs] == num_tokens) ? 1 : 0;
         s_base = make_int2(0, 0);
@@ -105,6 +106,10 @@ __global__ void __launch_bounds__(kPrepThreads) step_prep_kernel(
         page_off[num_reqs] = b.x;
         counters[1] = min(b.y, max_prefill_tiles);
     }
+    // This kernel reads nothing the previous one (kv_append) writes, so it ran alongside
+    // it; it finishes only after that kernel has, so that later kernels, which wait for
+    // this one, see the appended K/V.
+    grid_dep_wait();
 }
 
 }  // namespace
@@ -132,11 +137,11 @@ StepLayout make_step_layout(int num_reqs, int num_tokens) {
 
 cudaError_t launch_step_prep(const StepArgs& a, cudaStream_t stream) {
     const StepLayout& L = a.lay;
-    step_prep_kernel<<<1, kPrepThreads, 0, stream>>>(
-        a.cu_seqlens_q, a.context_lens, a.num_reqs, a.num_tokens, a.max_q_len, a.max_context_len,
-        a.max_blocks_per_seq, L.max_prefill_tiles, reinterpret_cast<int32_t*>(a.ws + L.counters_off),
-        reinterpret_cast<int32_t*>(a.ws + L.page_off_off), reinterpret_cast<int4*>(a.ws + L.prefill_tiles_off), a.err);
-    return cudaGetLastError();
+    return launch_pdl(step_prep_kernel, dim3(1), dim3(kPrepThreads), 0, stream, a.cu_seqlens_q, a.context_lens,
+                      a.num_reqs, a.num_tokens, a.max_q_len, a.max_context_len, a.max_blocks_per_seq,
+                      L.max_prefill_tiles, reinterpret_cast<int32_t*>(a.ws + L.counters_off),
+                      reinterpret_cast<int32_t*>(a.ws + L.page_off_off),
+                      reinterpret_cast<int4*>(a.ws + L.prefill_tiles_off), a.err);
 }
 
 }  // namespace kvp

@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
                                                         uint32_t* __restrict__ err) {
     __shared__ long long s_dst;  // element-chunk index of (block, head 0, slot) or -1
     __shared__ int s_req;
+    grid_dep_launch();   // the step's metadata kernel does not read the pool
     const int i = blockIdx.x;
     if (threadIdx.x == 0) s_req = -1;
     __syncthreads();

@@ -43,6 +43,14 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
+// ------------------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start before the
+// previous kernel in its stream has finished; grid_dep_wait() blocks until that kernel
+// has completed and its memory is visible.  grid_dep_launch() lets the next kernel of
+// the stream be scheduled early.  Both are no-ops for a normal launch.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 struct kvp_pool;
 
 namespace kvp {
@@ -60,6 +62,25 @@ cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const StepArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
                            const CUtensorMap* tmap_v, cudaStream_t stream);
+
+// Launch `kernel` so that it may start while the previous kernel of `stream` finishes
+// (programmatic dependent launch); the kernel must call grid_dep_wait() before it reads
+// what earlier kernels wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Device the pool's device-side state lives on, or -1 if it has none yet.
 int pool_device(const ::kvp_pool* p);
