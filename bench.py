@@ -3,7 +3,7 @@
 
 One step = one pass of the hot path over one packed batch: kv_append of the step's new
 K/V rows into the 16-token block pool, then paged_attention_step (metadata prep,
-tcgen05 prefill tiles, split-KV decode, combine), all through the C ABI.
+tcgen05 prefill tiles, split-KV decode with in-kernel merge), all through the C ABI.
 
 Metric: packed query tokens/s per attention layer (T / step time), and the decode
 kernel's KV-read GB/s against the measured HBM peak.  Default workload: the mixed
@@ -46,7 +46,7 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 L2_FLUSH_BYTES = 256 << 20
 CSRC = os.path.join(ROOT, "continuous_batching_paged_step_gb300", "csrc")
 KERNEL_SOURCES = {"decode_splitkv": "attn_decode.cu", "prefill_tcgen05": "attn_prefill.cu",
-                  "kv_append": "kv_append.cu", "step_prep": "attn_prep.cu", "splitkv_combine": "attn_decode.cu"}
+                  "kv_append": "kv_append.cu", "step_prep": "attn_prep.cu"}
 
 
 # ------------------------------------------------------------------ workload algebra
@@ -231,29 +231,37 @@ def run_gpu(a):
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     time.sleep(0.25)
-    kp.kv_pool_enable_timing(step.pool.handle, 8 * a.steps + 16)
+
+    def timed_steps(n):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        barrier()
+        torch.cuda.synchronize(dev)
+        for i in range(n):
+            flush.fill_((i + 1) & 0xFF)        # L2 flush between steps, outside the step's events
+            starts[i].record(stream)
+            step.run()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    # headline: the steps as a user runs them (no timing events inside the library calls)
     launches0 = kp.kv_pool_launch_count(step.pool.handle)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
-    barrier()
-    torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    for i in range(a.steps):
-        flush.fill_((i + 1) & 0xFF)        # L2 flush between steps, outside the step's events
-        starts[i].record(stream)
-        step.run()
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
-    barrier()
+    step_ms = timed_steps(a.steps)
     wall = time.perf_counter() - wall0
     launches = kp.kv_pool_launch_count(step.pool.handle) - launches0
+    # the same number of steps again with CUDA events around every kernel the library
+    # launches, on its launch stream: per-kernel durations for the roofline
+    kp.kv_pool_enable_timing(step.pool.handle, 8 * a.steps + 16)
+    step_ms_kernels = timed_steps(a.steps)
     per_kernel = kp.kv_pool_read_timing(step.pool.handle)
     kp.kv_pool_enable_timing(step.pool.handle, 0)
     clk = clocks.stop()
     st = step.error()
     if st != (0, 0):
         raise RuntimeError(f"device error word after the timed steps: {st}")
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
     if dist is not None:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
@@ -316,6 +324,7 @@ def run_gpu(a):
         "decode_kv_gbs": rl_decode["achieved"] if rl_decode else None,
         "roofline": roofline, "roofline_secondary": secondary,
         "kernels_us": {k: round(v["avg_us"], 2) for k, v in kern.items()},
+        "ms_per_step_with_kernel_events": round(sum(step_ms_kernels) / a.steps, 5),
         "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": int(launches),
         "wall_s_timed": round(wall, 3),
     }
@@ -402,13 +411,54 @@ def run_reference(a):
     return line
 
 
+def run_trace(a):
+    """The trace replay: 512 requests (Poisson arrivals, shared 1024-token system prompt in
+    refcounted blocks, lognormal prompts and outputs), FCFS under an 8192-token budget, a
+    40 GiB pool; every step is kv_append + paged_attention_step.  Reports packed tokens
+    over the summed GPU time of the steps (host scheduling and input generation are not
+    timed), the per-step distribution, and the decode KV bytes streamed."""
+    import torch
+    from continuous_batching_paged_step_gb300 import build as b
+    b.build()
+    from continuous_batching_paged_step_gb300 import kvpaged as kp
+    from continuous_batching_paged_step_gb300 import workloads as wl
+    from continuous_batching_paged_step_gb300.trace import TraceRunner
+    ts = wl.TraceSpec()
+    tr = TraceRunner(ts)
+    kp.kv_pool_enable_timing(tr.pool.handle, 8 * 4000)
+    w0 = time.perf_counter()
+    tr.run()
+    wall = time.perf_counter() - w0
+    per_kernel = kp.kv_pool_read_timing(tr.pool.handle)
+    st = kp.kv_pool_get_error(tr.pool.handle)
+    if st != (0, 0):
+        raise RuntimeError(f"device error word after the trace: {st}")
+    s = tr.summary()
+    hbm, bf16, _, peak_src = peaks()
+    n_dec, ms_dec = per_kernel["decode_splitkv"]
+    dec_gbs = s["decode_bytes"] / (ms_dec / 1e3) / 1e9 if ms_dec else None
+    line = {"metric": METRIC, "value": round(s["tokens_per_s"], 1), "unit": UNIT, "n_gpus": 1, "steps": s["steps"],
+            "warmup": 0, "ms_per_step": round(s["gpu_ms"] / max(1, s["steps"]), 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": ts.name, "requests": ts.n_requests, "shared_prefix": ts.shared_prefix,
+                       "budget": ts.budget, "kv_pool_blocks": ts.pool_blocks,
+                       "arrivals_per_step": ts.arrivals_per_step},
+            "trace": {k: (round(v, 4) if isinstance(v, float) else v) for k, v in s.items()},
+            "decode_kv_gbs": round(dec_gbs, 1) if dec_gbs else None,
+            "decode_kv_frac_of_hbm": round(dec_gbs / hbm, 4) if dec_gbs else None,
+            "kernels_ms_total": {k: round(v[1], 3) for k, v in per_kernel.items() if v[0]},
+            "wall_s": round(wall, 1)}
+    print(json.dumps(line), flush=True)
+    tr.close()
+
+
 def main():
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", choices=["mixed", "decode", "chunked", "tiny"], default="mixed")
+    p.add_argument("--config", choices=["mixed", "decode", "chunked", "tiny", "trace"], default="mixed")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--oracle-rows-per-chunk", type=int, default=256)
     a = p.parse_args()
@@ -416,6 +466,8 @@ def main():
         p.error("--warmup must be at least 3")
     if a.impl == "reference":
         run_reference(a)
+    elif a.config == "trace":
+        run_trace(a)
     else:
         run_gpu(a)
 

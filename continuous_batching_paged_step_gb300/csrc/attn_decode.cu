@@ -7,11 +7,11 @@
 // bandwidth-bound"), so the kernel is built to keep HBM busy:
 //
 // * Balanced split: the 16-token blocks of all decode rows, concatenated in request
-//   order (page_off[r] = first global block of request r), are cut into gridDim.x equal
-//   contiguous ranges, one per CTA (one CTA per SM).  A CTA walks its range request by
+//   order (page_off[r] = first global block of request r), are cut into equal contiguous
+//   ranges, one per CTA (one CTA per SM; fewer when there are under 4 blocks per CTA).  A CTA walks its range request by
 //   request; a request cut by a range boundary produces one partial per CTA that touches
-//   it (slot r + cta), merged afterwards by the combine kernel; a request inside one
-//   range is finished in place.  Every CTA streams the same number of blocks.
+//   it (slot r + cta), merged by whichever of those CTAs finishes last; a request inside
+//   one range is finished in place.  Every CTA streams the same number of blocks.
 // * One block of all 8 KV heads is 32 KiB contiguous in the pool, so each block of K and
 //   of V arrives with ONE bulk copy (cp.async.bulk, mbarrier completion, L2 evict-first)
 //   into a 3-stage shared-memory ring (64 KiB per stage).  Lane 0 of warp 0 issues the
@@ -25,8 +25,9 @@
 //   query is pre-scaled by softmax_scale * log2 e): running max m and sum l per head.
 // * P.V: a lane owns 4 output dims of all 4 heads; weights of the warp's 8 tokens go
 //   through a per-warp shared-memory slot as duplicated pairs for the packed FMAs.
-// Partial results keep (m, l, unnormalised acc); the combine is
-// O = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s with M = max_s m_s.
+// Partial results keep (m, l, unnormalised acc); the last CTA to finish a split row
+// (an arrival count per row) merges them: O = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M)
+// l_s with M = max_s m_s.
 // Keys at positions >= ctx + 1 of the last block are excluded (score -inf, value unread).
 #include "kvp_device.cuh"
 #include "kvp_launch.h"
@@ -58,6 +59,8 @@ struct __align__(128) DecodeSmem {
     float2 merge_acc[kNumKvHeads][32][8];             // second half's accumulators
     float merge_ml[kNumKvHeads][8];                   // second half's m[4], l[4]
     int pair_abort[kNumKvHeads];
+    int cta_abort;
+    int merge_last;
     int first_req;
     Producer prod;
     uint64_t full[kDecStages];
@@ -107,6 +110,15 @@ __device__ __forceinline__ void pv_token(const float2 (&pt)[kGroup], const uint8
     }
 }
 
+// A decode CTA streams at least this many blocks: with fewer blocks than CTAs x this,
+// only ceil(P / kMinBlocksPerCta) CTAs take part (fewer, longer segments to merge).
+constexpr int kMinBlocksPerCta = 4;
+
+__device__ __forceinline__ int effective_ctas(int P, int G) {
+    const int by_work = (P + kMinBlocksPerCta - 1) / kMinBlocksPerCta;
+    return max(1, min(G, by_work));
+}
+
 // Block range [lo, hi) of CTA c out of G over P blocks.
 __device__ __forceinline__ void cta_range(int P, int c, int G, int& lo, int& hi) {
     lo = (int)(((long long)P * c) / G);
@@ -149,20 +161,51 @@ __device__ __noinline__ void produce_next(DecodeSmem& S, const int32_t* __restri
     }
 }
 
+// Merge the partial results of a decode row whose blocks were split over CTAs c0..c1
+// (all 512 threads of the CTA: thread t takes query head t / 16 and dims 8 (t % 16) ..
+// 8 (t % 16) + 7).  O = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c.
+__device__ __noinline__ void merge_partials(int r, int row, int c0, int c1, const float* part_acc,
+                                            const float2* part_ml, __nv_bfloat16* out) {
+    const int head = threadIdx.x >> 4, d0 = (threadIdx.x & 15) * 8;
+    float M = -INFINITY;
+    for (int c = c0; c <= c1; ++c) M = fmaxf(M, __ldcg(&part_ml[((size_t)r + c) * kNumQHeads + head]).x);
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float L = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int c = c0; c <= c1; ++c) {
+        const size_t sh = ((size_t)r + c) * kNumQHeads + head;
+        const float2 ml = __ldcg(&part_ml[sh]);
+        const float w = fast_exp2(ml.x - Mu);
+        L = fmaf(ml.y, w, L);
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(part_acc + sh * kHeadDim + d0));
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(part_acc + sh * kHeadDim + d0 + 4));
+        o[0] = fmaf(a.x, w, o[0]); o[1] = fmaf(a.y, w, o[1]); o[2] = fmaf(a.z, w, o[2]); o[3] = fmaf(a.w, w, o[3]);
+        o[4] = fmaf(b.x, w, o[4]); o[5] = fmaf(b.y, w, o[5]); o[6] = fmaf(b.z, w, o[6]); o[7] = fmaf(b.w, w, o[7]);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint4 wv;
+    wv.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+    wv.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+    wv.z = pack_bf16x2(o[4] * inv, o[5] * inv);
+    wv.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+    *reinterpret_cast<uint4*>(out + (size_t)row * kQRowElems + head * kHeadDim + d0) = wv;
+}
+
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
     const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out, const int32_t* __restrict__ cu,
     const int32_t* __restrict__ ctx, const int32_t* __restrict__ tables, int max_blocks, int num_blocks,
     const uint8_t* __restrict__ k_cache, const uint8_t* __restrict__ v_cache, const int32_t* __restrict__ page_off,
-    int num_reqs, float* __restrict__ part_acc, float2* __restrict__ part_ml, float scale_log2,
-    uint32_t* __restrict__ err) {
+    int num_reqs, float* __restrict__ part_acc, float2* __restrict__ part_ml, int32_t* __restrict__ seg_count,
+    float scale_log2, uint32_t* __restrict__ err) {
     extern __shared__ uint8_t smem_raw[];
     DecodeSmem& S = *reinterpret_cast<DecodeSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     grid_dep_wait();     // block offsets, cache contents
     grid_dep_launch();
     const int P = page_off[num_reqs];
+    const int G = effective_ctas(P, gridDim.x);
+    if ((int)blockIdx.x >= G) return;
     int lo, hi;
-    cta_range(P, blockIdx.x, gridDim.x, lo, hi);
+    cta_range(P, blockIdx.x, G, lo, hi);
     if (lo >= hi) return;
 
     if (threadIdx.x == 0) {
@@ -181,6 +224,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
         S.first_req = a;
     }
     if (threadIdx.x < kNumKvHeads) S.pair_abort[threadIdx.x] = 0;
+    if (threadIdx.x == 0) S.cta_abort = 0;
     __syncthreads();
 
     const bool is_producer = (warp == 0 && lane == 0);
@@ -359,7 +403,28 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
             }
         }
         named_bar(1 + h, 64);
-        if (pair_aborted) break;
+        // The whole CTA agrees on abort before anyone leaves the loop (every warp walks the
+        // same segments, so every warp reaches these barriers).
+        if (pair_aborted && (warp & 1) == 0 && lane == 0) S.cta_abort = 1;
+        __syncthreads();
+        const bool cta_aborted = S.cta_abort != 0;
+        if (!whole && !cta_aborted) {
+            // Split row: count this CTA's partial in; the CTA that completes the count
+            // merges all of the row's partials (their writes are published by the fence
+            // before the count, and read past L1 after it).
+            if (threadIdx.x == 0) {
+                __threadfence();
+                const int c0 = owner_cta(req_lo, P, G), c1 = owner_cta(req_hi - 1, P, G);
+                const int old = atomicAdd(&seg_count[r], 1);
+                S.merge_last = (old == c1 - c0) ? 1 : 0;
+                if (S.merge_last) __threadfence();
+            }
+            __syncthreads();
+            if (S.merge_last) merge_partials(r, row, owner_cta(req_lo, P, G), owner_cta(req_hi - 1, P, G), part_acc,
+                                             part_ml, out);
+            __syncthreads();
+        }
+        if (cta_aborted) break;
         // next request that has blocks
         ++r;
         while (r + 1 <= num_reqs - 1 && page_off[r + 1] == page_off[r]) ++r;
@@ -380,44 +445,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
     }
 }
 
-// Merge the partials of decode rows whose blocks were split across CTAs: one CTA per
-// (request, group of 8 query heads), one warp per query head, a lane owns 4 dims.
-__global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict__ page_off, int num_reqs, int G,
-                                                      const int32_t* __restrict__ cu,
-                                                      const float* __restrict__ part_acc,
-                                                      const float2* __restrict__ part_ml,
-                                                      __nv_bfloat16* __restrict__ out) {
-    const int r = blockIdx.x;
-    grid_dep_wait();     // partials of the decode kernel
-    const int P = page_off[num_reqs];
-    const int a = page_off[r], b = page_off[r + 1];
-    if (b <= a) return;
-    const int c0 = owner_cta(a, P, G), c1 = owner_cta(b - 1, P, G);
-    if (c0 == c1) return;  // finished in place by its CTA
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int head = blockIdx.y * 8 + warp;
-    float M = -INFINITY;
-    for (int c = c0; c <= c1; ++c) M = fmaxf(M, part_ml[((size_t)r + c) * kNumQHeads + head].x);
-    const float Mu = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-    for (int c = c0; c <= c1; ++c) {
-        const size_t sh = ((size_t)r + c) * kNumQHeads + head;
-        const float2 ml = part_ml[sh];
-        const float w = fast_exp2(ml.x - Mu);
-        L = fmaf(ml.y, w, L);
-        const float4 v = *reinterpret_cast<const float4*>(part_acc + sh * kHeadDim + lane * 4);
-        o0 = fmaf(v.x, w, o0);
-        o1 = fmaf(v.y, w, o1);
-        o2 = fmaf(v.z, w, o2);
-        o3 = fmaf(v.w, w, o3);
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    uint2 wv;
-    wv.x = pack_bf16x2(o0 * inv, o1 * inv);
-    wv.y = pack_bf16x2(o2 * inv, o3 * inv);
-    *reinterpret_cast<uint2*>(out + (size_t)cu[r] * kQRowElems + head * kHeadDim + lane * 4) = wv;
-}
-
 int decode_grid(const StepArgs& a) {
     int g = a.num_sms > 0 ? a.num_sms : 1;
     if (g > kMaxDecodeCtas) g = kMaxDecodeCtas;
@@ -436,16 +463,7 @@ cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream) {
                       static_cast<const uint8_t*>(a.k_cache), static_cast<const uint8_t*>(a.v_cache),
                       reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs,
                       reinterpret_cast<float*>(a.ws + L.part_acc_off), reinterpret_cast<float2*>(a.ws + L.part_ml_off),
-                      a.softmax_scale * 1.4426950408889634f, a.err);
-}
-
-cudaError_t launch_combine(const StepArgs& a, cudaStream_t stream) {
-    const StepLayout& L = a.lay;
-    dim3 grid(a.num_reqs, kNumQHeads / 8);
-    return launch_pdl(combine_kernel, grid, dim3(256), 0, stream,
-                      reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs, decode_grid(a),
-                      a.cu_seqlens_q, reinterpret_cast<const float*>(a.ws + L.part_acc_off),
-                      reinterpret_cast<const float2*>(a.ws + L.part_ml_off), static_cast<__nv_bfloat16*>(a.out));
+                      reinterpret_cast<int32_t*>(a.ws + L.seg_count_off), a.softmax_scale * 1.4426950408889634f, a.err);
 }
 
 cudaError_t configure_decode_kernel() {

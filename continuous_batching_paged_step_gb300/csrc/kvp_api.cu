@@ -384,8 +384,6 @@ kvp_status paged_attention_step(kvp_pool* p, const void* q, void* out, const int
     }
     if (timed_launch(p, KVP_KERNEL_DECODE, s, [&] { return kvp::launch_decode(a, s); }) != cudaSuccess)
         return KVP_E_CUDA;
-    if (timed_launch(p, KVP_KERNEL_COMBINE, s, [&] { return kvp::launch_combine(a, s); }) != cudaSuccess)
-        return KVP_E_CUDA;
     return KVP_OK;
 }
 

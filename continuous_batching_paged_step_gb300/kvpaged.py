@@ -45,7 +45,7 @@ SIGNATURES = {
     "paged_attention_step_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "paged_attention_noalloc_capacity": (_SZ, []),
 }
-KERNEL_NAMES = ("kv_append", "step_prep", "prefill_tcgen05", "decode_splitkv", "splitkv_combine")
+KERNEL_NAMES = ("kv_append", "step_prep", "prefill_tcgen05", "decode_splitkv")
 
 
 class KVPError(RuntimeError):

@@ -27,7 +27,7 @@ def _dev_i32(a: np.ndarray, device) -> torch.Tensor:
 
 class PagedStep:
     def __init__(self, inp: StepInputs, device="cuda", pool_fill_bits: int | None = None,
-                 decode_ctas: int | None = None, fill_prior: bool = True):
+                 decode_ctas: int | None = None, fill_prior: bool = True, poison_workspace: bool = False):
         spec = inp.spec
         self.inp = inp
         self.device = device
@@ -52,6 +52,8 @@ class PagedStep:
         ws = kp.paged_attention_workspace_size(self.pool.handle, spec.num_reqs, spec.num_tokens,
                                                self.max_context_len)
         self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
+        if poison_workspace:
+            self.workspace.fill_(0x5A)        # stale-looking bytes: nothing may read scratch it did not write
         if fill_prior:
             self.write_prior()
 

@@ -201,3 +201,65 @@ CONFIGS = {
     "decode": decode_heavy_step,
     "chunked": chunked_prefill_step,
 }
+
+
+# --------------------------------------------------------------------------------------
+# Trace replay: a stream of requests arriving over steps.  Lengths follow the shapes named
+# for the method's workloads (page "11.2 连续批处理与 PagedAttention", sections 11.2.2-11.2.5):
+# a shared system prompt, skewed prompt and output lengths.  Values the pages leave open
+# (arrival rate, lognormal sigmas) are fixed here and recorded with the design.
+# --------------------------------------------------------------------------------------
+
+@dataclass
+class TraceSpec:
+    name: str = "trace-512req"
+    n_requests: int = 512
+    arrivals_per_step: float = 4.0        # Poisson rate on the step clock
+    shared_prefix: int = 1024             # tokens of the shared system prompt (full blocks)
+    prompt_median: float = 256.0
+    prompt_sigma: float = 1.0
+    prompt_cap: int = 4096
+    output_median: float = 100.0
+    output_sigma: float = 1.0
+    output_range: tuple = (10, 2000)
+    budget: int = 8192                    # tokens per step, decode rows first
+    max_num_seqs: int = 0                 # 0: no limit on running requests
+    pool_blocks: int = 655360             # 40 GiB of K+V for one layer
+    seed: int = 0xC0FFEE + 5
+
+
+@dataclass
+class TraceRequest:
+    rid: int
+    arrival: int          # step at which the request becomes visible to the scheduler
+    prompt_len: int       # own prompt tokens, after the shared prefix
+    output_len: int       # tokens the request generates (the first comes with its last prefill chunk)
+
+
+def make_trace(ts: TraceSpec) -> list:
+    rng = np.random.default_rng([ts.seed, 0x7EACE])
+    reqs, step = [], 0
+    while len(reqs) < ts.n_requests:
+        for _ in range(int(rng.poisson(ts.arrivals_per_step))):
+            if len(reqs) == ts.n_requests:
+                break
+            p = int(np.clip(np.round(np.exp(math.log(ts.prompt_median) + ts.prompt_sigma * rng.standard_normal())),
+                            1, ts.prompt_cap))
+            o = int(np.clip(np.round(np.exp(math.log(ts.output_median) + ts.output_sigma * rng.standard_normal())),
+                            ts.output_range[0], ts.output_range[1]))
+            reqs.append(TraceRequest(len(reqs), step, p, o))
+        step += 1
+    return reqs
+
+
+_TRACE_Q, _TRACE_K, _TRACE_V = 11, 12, 13
+
+
+def trace_rows(seed: int, rid: int, start: int, n: int, n_q: int = N_Q_HEADS * HEAD_DIM,
+               n_kv: int = N_KV_HEADS * HEAD_DIM):
+    """Q, K and V rows (bf16 bits) of the n tokens a request feeds from position `start`.
+    rid = -1 is the shared system prompt.  Each (request, start) chunk has its own stream,
+    so any chunk can be regenerated alone."""
+    return (_normal_bf16(seed, rid + 1, _TRACE_Q * 100003 + start, (n, n_q)),
+            _normal_bf16(seed, rid + 1, _TRACE_K * 100003 + start, (n, n_kv)),
+            _normal_bf16(seed, rid + 1, _TRACE_V * 100003 + start, (n, n_kv)))

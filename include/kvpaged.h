@@ -231,9 +231,8 @@ KVP_API size_t paged_attention_noalloc_capacity(void);
 #define KVP_KERNEL_APPEND  0
 #define KVP_KERNEL_PREP    1
 #define KVP_KERNEL_PREFILL 2
-#define KVP_KERNEL_DECODE  3
-#define KVP_KERNEL_COMBINE 4
-#define KVP_NUM_KERNELS    5
+#define KVP_KERNEL_DECODE  3   /* split-KV partials are merged inside this kernel */
+#define KVP_NUM_KERNELS    4
 KVP_API kvp_status kv_pool_enable_timing(kvp_pool* pool, int max_launches);
 KVP_API kvp_status kv_pool_read_timing(kvp_pool* pool, int* counts, float* ms);
 

@@ -59,7 +59,7 @@ def _pool_bits(step):
 
 def _run_full_check(runner, spec, ctas=None):
     inp = wl.make_inputs(spec)
-    step = runner.PagedStep(inp, pool_fill_bits=NAN_BITS, decode_ctas=ctas)
+    step = runner.PagedStep(inp, pool_fill_bits=NAN_BITS, decode_ctas=ctas, poison_workspace=True)
     try:
         step.run()
         st, bits = step.error()
