@@ -196,16 +196,11 @@ def run_gpu(a):
     from continuous_batching_paged_step_gb300 import kvpaged as kp
     from continuous_batching_paged_step_gb300 import runner, workloads as wl
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from continuous_batching_paged_step_gb300 import replicas
+    rank, world, local = replicas.dist_env()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    dist = replicas.init("nccl", device=dev)
 
     spec = wl.CONFIGS[a.config]()
     inp = wl.make_inputs(spec)
@@ -216,8 +211,7 @@ def run_gpu(a):
     work = work_of(spec)
 
     def barrier():
-        if dist is not None:
-            dist.barrier()
+        replicas.barrier(dist)
 
     # warm-up
     for i in range(a.warmup):
@@ -262,12 +256,8 @@ def run_gpu(a):
     st = step.error()
     if st != (0, 0):
         raise RuntimeError(f"device error word after the timed steps: {st}")
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * T * a.steps / (total_ms / 1e3)
+    total_ms = replicas.max_over_ranks(dist, sum(step_ms), device=dev)
+    value = replicas.aggregate_rate(T * a.steps, world, total_ms)
 
     # ----------------------------------------------------------- end to end (host buffers)
     e2e = run_e2e(a, step, stream, dev, flush, dist, world)
@@ -336,42 +326,66 @@ def run_gpu(a):
 
 
 def run_e2e(a, step, stream, dev, flush, dist, world):
-    """Same metric through the C ABI with host buffers: H2D of the step's inputs from pinned
-    memory, the step, D2H of the output, all inside the events."""
+    """Same metric through the C ABI with host buffers, as a serving loop runs it: every
+    step's inputs go host -> device from pinned memory and its output device -> host,
+    inside the timed region.  The copies are pipelined with the compute: two sets of
+    device inputs/outputs, uploads on one stream, downloads on another, so step i+1's
+    upload and step i-1's download overlap step i's kernels.  No L2 flush here: every
+    step streams the decode rows' whole KV history (hundreds of MB, more than L2)."""
     import torch
+    from continuous_batching_paged_step_gb300 import kvpaged as kp
+    from continuous_batching_paged_step_gb300 import replicas
     inp = step.inp
     names = ("q", "k_new", "v_new", "cu_seqlens_q", "context_lens", "block_tables")
     host = {n: getattr(step, n).cpu().pin_memory() for n in names}
-    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    out_h = [torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory() for _ in range(2)]
+    bufs = [{n: torch.empty_like(getattr(step, n)) for n in names} for _ in range(2)]
+    outs = [torch.empty_like(step.out) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_h.numel() * out_h.element_size()
-    n = max(3, a.steps // 4)
+    d2h = out_h[0].numel() * out_h[0].element_size()
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    n = max(4, a.steps // 4)
 
-    def one():
-        for nm in names:
-            getattr(step, nm).copy_(host[nm], non_blocking=True)
-        step.run()
-        out_h.copy_(step.out, non_blocking=True)
+    def run(count, timed):
+        done = [None] * count
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        if timed:
+            t0.record(up)
+        for i in range(count):
+            b = bufs[i % 2]
+            if i >= 2:
+                up.wait_event(done[i - 2])          # the set is free once step i-2 finished
+            with torch.cuda.stream(up):
+                for nm in names:
+                    b[nm].copy_(host[nm], non_blocking=True)
+                loaded = torch.cuda.Event()
+                loaded.record(up)
+            stream.wait_event(loaded)
+            kp.kv_append(step.pool.handle, b["k_new"], b["v_new"], b["cu_seqlens_q"], b["context_lens"],
+                         b["block_tables"], stream=stream)
+            kp.paged_attention_step(step.pool.handle, b["q"], outs[i % 2], b["cu_seqlens_q"], b["context_lens"],
+                                    b["block_tables"], step.max_q_len, step.max_context_len, step.softmax_scale,
+                                    step.workspace, stream=stream)
+            computed = torch.cuda.Event()
+            computed.record(stream)
+            down.wait_event(computed)
+            with torch.cuda.stream(down):
+                out_h[i % 2].copy_(outs[i % 2], non_blocking=True)
+                fin = torch.cuda.Event()
+                fin.record(down)
+            done[i] = fin
+        if timed:
+            t1.record(down)
+        torch.cuda.synchronize(dev)
+        return t0.elapsed_time(t1) if timed else 0.0
 
-    for i in range(3):
-        one()
-    torch.cuda.synchronize(dev)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-    for i in range(n):
-        flush.fill_(i & 0xFF)
-        starts[i].record(stream)
-        one()
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
-    total = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
-    if dist is not None:
-        t = torch.tensor([total], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total = float(t.item())
+    run(4, False)
+    total = replicas.max_over_ranks(dist, run(n, True), device=dev)
     T = inp.spec.num_tokens
-    return {"value": round(world * T * n / (total / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": n}
+    return {"value": round(replicas.aggregate_rate(T * n, world, total), 1), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,
+            "pipelining": "double-buffered device inputs/outputs; uploads, kernels and downloads on three streams"}
 
 
 # ---------------------------------------------------------------- reference arm
