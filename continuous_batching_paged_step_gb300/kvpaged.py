@@ -44,6 +44,7 @@ SIGNATURES = {
     "kv_pool_launch_count": (ctypes.c_longlong, [_P]),
     "paged_attention_step_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "paged_attention_noalloc_capacity": (_SZ, []),
+    "kvp_selftest_bounded_wait": (_I, [ctypes.c_longlong, _P]),
 }
 KERNEL_NAMES = ("kv_append", "step_prep", "prefill_tcgen05", "decode_splitkv")
 
@@ -179,6 +180,12 @@ def kv_pool_read_timing(pool: int):
 
 def kv_pool_launch_count(pool: int) -> int:
     return lib.kv_pool_launch_count(pool)
+
+
+def kvp_selftest_bounded_wait(limit_ns: int, stream=None) -> int:
+    """Make one bounded device wait run out on purpose; returns the status (KVP_E_TIMEOUT
+    when the wait gave up as it should)."""
+    return lib.kvp_selftest_bounded_wait(int(limit_ns), _stream(stream))
 
 
 # ------------------------------------------------------------------ the step

@@ -239,6 +239,14 @@ KVP_API kvp_status kv_pool_read_timing(kvp_pool* pool, int* counts, float* ms);
 /* Number of kernels this pool's calls have launched so far (host counter). */
 KVP_API long long kv_pool_launch_count(const kvp_pool* pool);
 
+/* Make one bounded device wait run out on purpose: a single thread waits on an mbarrier
+ * that nothing arrives at, for limit_ns nanoseconds (0 < limit_ns <= 2e9), on `stream`
+ * (synchronised before returning).  Returns KVP_E_TIMEOUT when the wait gave up as it
+ * should (the same bounded-wait mechanism the step's kernels use, which then set
+ * KVP_ERRBIT_TIMEOUT and finish), KVP_OK if the barrier completed (it cannot), or
+ * KVP_E_INVALID_ARG / KVP_E_CUDA.  Faults and hangs nothing; allocates 4 bytes. */
+KVP_API kvp_status kvp_selftest_bounded_wait(long long limit_ns, kvp_stream stream);
+
 /* Human-readable name of a status code (static storage). */
 KVP_API const char* kvp_status_string(kvp_status s);
 

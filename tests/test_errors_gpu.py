@@ -112,3 +112,22 @@ def test_host_argument_errors(mods):
         assert step.error() == (0, 0)      # nothing was launched
     finally:
         step.close()
+
+
+def test_bounded_wait_gives_up_and_the_context_survives(mods):
+    # A wait that nothing completes gives up after its limit and reports it; the GPU
+    # context stays usable (a full step afterwards is still correct).
+    import time
+    kp, runner = mods
+    t0 = time.perf_counter()
+    assert kp.kvp_selftest_bounded_wait(50_000_000) == -9          # KVP_E_TIMEOUT after ~50 ms
+    assert time.perf_counter() - t0 < 5.0
+    inp = wl.make_inputs(wl.tiny_p5_step())
+    step = runner.PagedStep(inp)
+    try:
+        step.run()
+        assert step.error() == (0, 0)
+        want = oracle.step_reference(inp)
+        assert np.abs(step.out_f32() - want).max() <= 2e-2
+    finally:
+        step.close()
