@@ -8,21 +8,26 @@
 //
 // * Balanced split: the 16-token blocks of all decode rows, concatenated in request
 //   order (page_off[r] = first global block of request r), are cut into equal contiguous
-//   ranges, one per CTA (one CTA per SM; fewer when there are under 4 blocks per CTA).  A CTA walks its range request by
-//   request; a request cut by a range boundary produces one partial per CTA that touches
-//   it (slot r + cta), merged by whichever of those CTAs finishes last; a request inside
-//   one range is finished in place.  Every CTA streams the same number of blocks.
+//   ranges, one per CTA (one CTA per SM; fewer when there are under 4 blocks per CTA; more
+//   CTAs, in whole waves, when a range would exceed the 2,048 block ids a CTA stages).  A
+//   CTA walks its range request by request; a request cut by a range boundary produces one
+//   partial per CTA that touches it (slot r + cta), merged by whichever of those CTAs
+//   finishes last; a request inside one range is finished in place.
+// * The CTA first looks up the physical ids of all its blocks in parallel (into shared
+//   memory), so no table lookup sits between a freed buffer and its refill.
 // * One block of all 8 KV heads is 32 KiB contiguous in the pool, so each block of K and
-//   of V arrives with ONE bulk copy (cp.async.bulk, mbarrier completion, L2 evict-first)
-//   into a 3-stage shared-memory ring (64 KiB per stage).  Lane 0 of warp 0 issues the
-//   copies: after its warp has consumed a stage it refills it with the block three ahead.
+//   of V arrives with ONE bulk copy (cp.async.bulk, mbarrier completion) into a 3-stage
+//   ring of 64 KiB stages; the last of the 16 warps to finish with a stage refills it
+//   with the block three ahead (no thread waits for the others to do so).
 // * GQA packing: the 4 query heads of a KV head share every K/V byte read.  Two warps
 //   per KV head (16 warps) split each block's 16 tokens 8/8, with separate
 //   online-softmax states merged at the end of a request segment.
 // * Scores: a lane holds 16 of the 128 dims (8 lanes per token) of 2 tokens for all 4
 //   query heads; packed fp32x2 FMAs; a transpose-reduce over the 8 lanes (7 shuffles)
 //   leaves one finished (token, head) score per lane.  Online softmax in base 2 (the
-//   query is pre-scaled by softmax_scale * log2 e): running max m and sum l per head.
+//   query is pre-scaled by softmax_scale * log2 e) against a reference max per head that
+//   moves only when a score exceeds it by more than 2^8 (a warp vote; the max reduction
+//   and the rescale run only then), with per-lane partial sums reduced once per segment.
 // * P.V: a lane owns 4 output dims of all 4 heads; weights of the warp's 8 tokens go
 //   through a per-warp shared-memory slot as duplicated pairs for the packed FMAs.
 // Partial results keep (m, l, unnormalised acc); the last CTA to finish a split row
@@ -41,19 +46,11 @@ constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDecStages = 3;
 constexpr int kTokensPerWarp = kBlockSize / 2;
 
-// Producer cursor over the CTA's blocks (used by lane 0 of warp 0 only; kept in shared
-// memory so the other 511 threads do not carry its registers).
-struct Producer {
-    int r, page, hi;
-    int stage;
-    uint32_t phase;
-    int issued;
-    int ok;
-    uint64_t policy;
-};
+constexpr int kIdCap = 2048;   // block ids a CTA stages in shared memory (its whole range)
 
 struct __align__(128) DecodeSmem {
-    uint8_t kv[kDecStages][2][kBlockBytes];          // [stage][K|V][8 heads x 16 x 128 bf16]
+    uint8_t kv[kDecStages][2][kBlockBytes];           // [stage][K|V][8 heads x 16 x 128 bf16]
+    int32_t ids[kIdCap];                              // physical block of each block of the range
     float2 pbuf[kDecWarps][kTokensPerWarp][kGroup];   // (p, p) per token and head
     float2 abuf[kDecWarps][kGroup];                   // (alpha, alpha) per head
     float2 merge_acc[kNumKvHeads][32][8];             // second half's accumulators
@@ -61,8 +58,13 @@ struct __align__(128) DecodeSmem {
     int pair_abort[kNumKvHeads];
     int cta_abort;
     int merge_last;
-    int first_req;
-    Producer prod;
+    int first_req, last_req;
+    unsigned released[kDecStages];                    // warps done with a stage (mod 16)
+    int issued;                                       // blocks issued so far
+    int n_rel;                                        // blocks in the range
+    const uint8_t* cache[2];                          // K and V pools
+    uint32_t* err;
+    uint64_t policy;
     uint64_t full[kDecStages];
     uint64_t empty[kDecStages];
 };
@@ -114,9 +116,13 @@ __device__ __forceinline__ void pv_token(const float2 (&pt)[kGroup], const uint8
 // only ceil(P / kMinBlocksPerCta) CTAs take part (fewer, longer segments to merge).
 constexpr int kMinBlocksPerCta = 4;
 
-__device__ __forceinline__ int effective_ctas(int P, int G) {
-    const int by_work = (P + kMinBlocksPerCta - 1) / kMinBlocksPerCta;
-    return max(1, min(G, by_work));
+// CTAs that share P blocks: at most `wave` at a time (one per SM), each range at most
+// kIdCap blocks (whole extra waves when P needs them).  0 when the launch is too small.
+__device__ __forceinline__ int decode_ctas_used(int P, int wave, int grid) {
+    const int per_wave = max(1, min(wave, (P + kMinBlocksPerCta - 1) / kMinBlocksPerCta));
+    const long long waves = max(1LL, ((long long)P + (long long)per_wave * kIdCap - 1) / ((long long)per_wave * kIdCap));
+    const long long G = waves * per_wave;
+    return G > grid ? 0 : (int)G;
 }
 
 // Block range [lo, hi) of CTA c out of G over P blocks.
@@ -131,34 +137,29 @@ __device__ __forceinline__ int owner_cta(int x, int P, int G) {
 }
 
 
-__device__ __noinline__ void produce_next(DecodeSmem& S, const int32_t* __restrict__ page_off, int num_reqs,
-                                          const int32_t* __restrict__ tables, int max_blocks, int num_blocks,
-                                          const uint8_t* __restrict__ k_cache, const uint8_t* __restrict__ v_cache,
-                                          uint32_t* __restrict__ err) {
-    Producer& pr = S.prod;
-    if (!pr.ok || pr.page >= pr.hi) return;
-    const int req_lo = page_off[pr.r];
-    int b = tables[(size_t)pr.r * max_blocks + (pr.page - req_lo)];
-    if ((unsigned)b >= (unsigned)num_blocks) {
-        raise_error(err, kErrBadBlock);
-        b = 0;
-    }
-    if (!mbar_wait(&S.empty[pr.stage], pr.phase ^ 1)) {
-        raise_error(err, kErrTimeout);
-        pr.ok = 0;
+// Copy K and V of block `q` of the range into stage `st`.
+__device__ __noinline__ void issue_block(DecodeSmem& S, int st, int q) {
+    const size_t off = (size_t)S.ids[q] * kBlockBytes;
+    mbar_arrive_expect_tx(&S.full[st], 2 * kBlockBytes);
+    bulk_load(S.kv[st][0], S.cache[0] + off, kBlockBytes, &S.full[st], S.policy);
+    bulk_load(S.kv[st][1], S.cache[1] + off, kBlockBytes, &S.full[st], S.policy);
+    atomicMax(&S.issued, q + 1);
+}
+
+// Lane 0 of a warp that is done reading block `rel` (stage st, phase ph): the last of
+// the 16 warps refills the stage with block rel + kDecStages.
+__device__ __forceinline__ void release_stage(DecodeSmem& S, int st, uint32_t ph, int rel) {
+    mbar_arrive(&S.empty[st]);
+    const unsigned old = atomicAdd(&S.released[st], 1u);
+    if ((old & (kDecWarps - 1)) != kDecWarps - 1) return;
+    const int q = rel + kDecStages;
+    if (q >= S.n_rel) return;
+    // every warp has arrived (or is about to): the wait only orders their reads before the copy
+    if (!mbar_wait(&S.empty[st], ph)) {
+        raise_error(S.err, kErrTimeout);
         return;
     }
-    mbar_arrive_expect_tx(&S.full[pr.stage], 2 * kBlockBytes);
-    bulk_load(S.kv[pr.stage][0], k_cache + (size_t)b * kBlockBytes, kBlockBytes, &S.full[pr.stage], pr.policy);
-    bulk_load(S.kv[pr.stage][1], v_cache + (size_t)b * kBlockBytes, kBlockBytes, &S.full[pr.stage], pr.policy);
-    ++pr.issued;
-    if (++pr.stage == kDecStages) {
-        pr.stage = 0;
-        pr.phase ^= 1;
-    }
-    if (++pr.page < pr.hi) {
-        while (pr.r + 1 < num_reqs && page_off[pr.r + 1] <= pr.page) ++pr.r;
-    }
+    issue_block(S, st, q);
 }
 
 // Merge the partial results of a decode row whose blocks were split over CTAs c0..c1
@@ -194,44 +195,76 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
     const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out, const int32_t* __restrict__ cu,
     const int32_t* __restrict__ ctx, const int32_t* __restrict__ tables, int max_blocks, int num_blocks,
     const uint8_t* __restrict__ k_cache, const uint8_t* __restrict__ v_cache, const int32_t* __restrict__ page_off,
-    int num_reqs, float* __restrict__ part_acc, float2* __restrict__ part_ml, int32_t* __restrict__ seg_count,
-    float scale_log2, uint32_t* __restrict__ err) {
+    int num_reqs, int wave, float* __restrict__ part_acc, float2* __restrict__ part_ml,
+    int32_t* __restrict__ seg_count, float scale_log2, uint32_t* __restrict__ err) {
     extern __shared__ uint8_t smem_raw[];
     DecodeSmem& S = *reinterpret_cast<DecodeSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     grid_dep_wait();     // block offsets, cache contents
     grid_dep_launch();
     const int P = page_off[num_reqs];
-    const int G = effective_ctas(P, gridDim.x);
+    if (P <= 0) return;
+    const int G = decode_ctas_used(P, wave, gridDim.x);
+    if (G == 0) {
+        // the launch has too few CTAs for this many blocks (the host sizes it from an
+        // upper bound, so this means inconsistent metadata)
+        if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(err, kErrBadMeta);
+        return;
+    }
     if ((int)blockIdx.x >= G) return;
     int lo, hi;
     cta_range(P, blockIdx.x, G, lo, hi);
     if (lo >= hi) return;
+    const int n_rel = hi - lo;   // <= kIdCap by construction of G
+    if (n_rel > kIdCap) {
+        if (threadIdx.x == 0) raise_error(err, kErrBadMeta);
+        return;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(&S.full[s], 1);
             mbar_init(&S.empty[s], kDecWarps);
+            S.released[s] = 0;
         }
+        S.issued = 0;
+        S.n_rel = n_rel;
+        S.cache[0] = k_cache;
+        S.cache[1] = v_cache;
+        S.err = err;
+        S.policy = policy_evict_first();
+        S.cta_abort = 0;
         fence_barrier_init();
-        // request holding block lo: the last r with page_off[r] <= lo
-        int a = 0, b = num_reqs;  // page_off[a] <= lo < page_off[b]
-        while (b - a > 1) {
-            const int mid = (a + b) >> 1;
-            if (page_off[mid] <= lo) a = mid;
-            else b = mid;
-        }
-        S.first_req = a;
     }
     if (threadIdx.x < kNumKvHeads) S.pair_abort[threadIdx.x] = 0;
-    if (threadIdx.x == 0) S.cta_abort = 0;
+    // requests holding the first and the last block of the range (one parallel pass)
+    for (int r = threadIdx.x; r < num_reqs; r += kDecThreads) {
+        const int a0 = page_off[r], a1 = page_off[r + 1];
+        if (a0 <= lo && lo < a1) S.first_req = r;
+        if (a0 <= hi - 1 && hi - 1 < a1) S.last_req = r;
+    }
     __syncthreads();
-
-    const bool is_producer = (warp == 0 && lane == 0);
-    if (is_producer) {
-        S.prod = Producer{S.first_req, lo, hi, 0, 0, 0, 1, policy_evict_first()};
-        for (int s = 0; s < kDecStages; ++s)
-            produce_next(S, page_off, num_reqs, tables, max_blocks, num_blocks, k_cache, v_cache, err);
+    // physical id of every block of the range
+    {
+        const int r_first = S.first_req, r_last = S.last_req;
+        for (int x = lo + threadIdx.x; x < hi; x += kDecThreads) {
+            int ra = r_first, rb = r_last;   // largest r with page_off[r] <= x
+            while (ra < rb) {
+                const int mid = (ra + rb + 1) >> 1;
+                if (page_off[mid] <= x) ra = mid;
+                else rb = mid - 1;
+            }
+            int b = tables[(size_t)ra * max_blocks + (x - page_off[ra])];
+            if ((unsigned)b >= (unsigned)num_blocks) {
+                raise_error(err, kErrBadBlock);
+                b = 0;
+            }
+            S.ids[x - lo] = b;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int j = 0; j < kDecStages && j < n_rel; ++j) issue_block(S, j, j);
     }
 
     const int h = warp >> 1, half = warp & 1;
@@ -264,7 +297,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
                 q2[g][i] = make_float2(f.x * scale_log2, f.y * scale_log2);
             }
         }
-        float m_own = -INFINITY, l_own = 0.f;
+        float m_ref = -INFINITY, l_part = 0.f;   // per head hd (m_ref uniform over its lanes)
         float2 acc[kGroup][2];
 #pragma unroll
         for (int g = 0; g < kGroup; ++g) acc[g][0] = acc[g][1] = make_float2(0.f, 0.f);
@@ -276,7 +309,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
             }
             if (!aborted) {
                 const uint8_t* kt = S.kv[stage][0] + h * kTileBytes + half * kTokensPerWarp * kHeadBytes;
-                const uint8_t* vt = S.kv[stage][1] + h * kTileBytes + half * kTokensPerWarp * kHeadBytes;
                 const int pos0 = (page - req_lo) * kBlockSize + half * kTokensPerWarp;
                 const int n_valid = min(kTokensPerWarp, n_keys - pos0);   // >= 1 except in a last block
                 // ---- scores of tokens tl and 4 + tl, all 4 heads
@@ -305,26 +337,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
                 float sc = b0 ? u1 : u0;
                 sc += __shfl_xor_sync(0xffffffffu, b0 ? u0 : u1, 1);
                 if (my_tok >= n_valid) sc = -INFINITY;
-                // ---- online softmax for head hd over the warp's 8 tokens
-                float mx = sc;
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float m_new = fmaxf(m_own, mx);
-                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                const float alpha = fast_exp2(m_own - m_use);
-                const float p = fast_exp2(sc - m_use);
-                float ps = p;
-                ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-                ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-                ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-                l_own = l_own * alpha + ps;
-                m_own = m_new;
-                S.pbuf[warp][my_tok][hd] = make_float2(p, p);
-                if ((lane & 0x19) == 0) S.abuf[warp][hd] = make_float2(alpha, alpha);
-                __syncwarp();
-                // ---- rescale and accumulate P.V (lane owns dims 4*lane .. 4*lane+3)
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                // ---- online softmax for head hd over the warp's 8 tokens.  The reference
+                // max m_ref moves only when a score exceeds it by more than 2^8 (then the
+                // warp reduces the max and rescales); the sum stays a per-lane partial
+                // until the segment ends.  Weights are 2^(s - m_ref) <= 2^8.
+                if (__any_sync(0xffffffffu, sc > m_ref + 8.f)) {
+                    float mx = sc;
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    const float m_new = fmaxf(m_ref, mx);
+                    const float alpha = fast_exp2(m_ref - (m_new == -INFINITY ? 0.f : m_new));
+                    l_part *= alpha;
+                    m_ref = m_new;
+                    if ((lane & 0x19) == 0) S.abuf[warp][hd] = make_float2(alpha, alpha);
+                    __syncwarp();
                     const float4 al01 = *reinterpret_cast<const float4*>(&S.abuf[warp][0]);
                     const float4 al23 = *reinterpret_cast<const float4*>(&S.abuf[warp][2]);
                     const float2 al[4] = {make_float2(al01.x, al01.y), make_float2(al01.z, al01.w),
@@ -335,29 +362,39 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
                         acc[g][1] = __fmul2_rn(acc[g][1], al[g]);
                     }
                 }
-                if (n_valid == kTokensPerWarp) {
-#pragma unroll
-                    for (int t = 0; t < kTokensPerWarp; ++t) pv_token(S.pbuf[warp][t], vt + t * kHeadBytes, lane, acc);
-                } else {
-                    for (int t = 0; t < n_valid; ++t) pv_token(S.pbuf[warp][t], vt + t * kHeadBytes, lane, acc);
-                }
+                const float p = fast_exp2(sc - (m_ref == -INFINITY ? 0.f : m_ref));
+                l_part += p;
+                S.pbuf[warp][my_tok][hd] = make_float2(p, p);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&S.empty[stage]);
+                {
+                    const uint8_t* vt = S.kv[stage][1] + h * kTileBytes + half * kTokensPerWarp * kHeadBytes;
+                    if (n_valid == kTokensPerWarp) {
+#pragma unroll
+                        for (int t = 0; t < kTokensPerWarp; ++t)
+                            pv_token(S.pbuf[warp][t], vt + t * kHeadBytes, lane, acc);
+                    } else {
+                        for (int t = 0; t < n_valid; ++t) pv_token(S.pbuf[warp][t], vt + t * kHeadBytes, lane, acc);
+                    }
+                    __syncwarp();
+                    if (lane == 0) release_stage(S, stage, phase, page - lo);
+                }
             }
             if (++stage == kDecStages) {
                 stage = 0;
                 phase ^= 1;
             }
-            if (is_producer) produce_next(S, page_off, num_reqs, tables, max_blocks, num_blocks, k_cache, v_cache, err);
         }
 
         // ------------------------------------------------ merge the two token halves
+        l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
+        l_part += __shfl_xor_sync(0xffffffffu, l_part, 8);
+        l_part += __shfl_xor_sync(0xffffffffu, l_part, 16);
         float m[kGroup], l[kGroup];
 #pragma unroll
         for (int g = 0; g < kGroup; ++g) {
             const int src = ((g >> 1) << 2) | ((g & 1) << 1);
-            m[g] = __shfl_sync(0xffffffffu, m_own, src);
-            l[g] = __shfl_sync(0xffffffffu, l_own, src);
+            m[g] = __shfl_sync(0xffffffffu, m_ref, src);
+            l[g] = __shfl_sync(0xffffffffu, l_part, src);
         }
         if (aborted && lane == 0) S.pair_abort[h] = 1;
         if (half == 1) {
@@ -430,26 +467,36 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
         while (r + 1 <= num_reqs - 1 && page_off[r + 1] == page_off[r]) ++r;
     }
 
-    if (is_producer) {
-        // Drain: the CTA must not retire while a copy still targets its shared memory.
-        const Producer& pr = S.prod;
-        for (int k = 1; k <= kDecStages && k <= pr.issued; ++k) {
-            int s = pr.stage - k;
-            uint32_t ph = pr.phase;
-            if (s < 0) {
-                s += kDecStages;
-                ph ^= 1;
-            }
-            if (!mbar_wait(&S.full[s], ph)) raise_error(err, kErrTimeout);
-        }
+    // Drain: the CTA must not retire while a copy still targets its shared memory (only
+    // possible after a wait ran out; otherwise every issued block was consumed).
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int n = S.issued;
+        for (int j = max(0, n - kDecStages); j < n; ++j)
+            if (!mbar_wait(&S.full[j % kDecStages], (uint32_t)((j / kDecStages) & 1))) raise_error(err, kErrTimeout);
     }
 }
 
-int decode_grid(const StepArgs& a) {
-    int g = a.num_sms > 0 ? a.num_sms : 1;
-    if (g > kMaxDecodeCtas) g = kMaxDecodeCtas;
-    if (a.decode_ctas > 0 && a.decode_ctas < g) g = a.decode_ctas;
-    return g;
+// CTAs that run at once: one per SM, or fewer when the pool asks for fewer.
+int decode_wave(const StepArgs& a) {
+    int w = a.num_sms > 0 ? a.num_sms : 1;
+    if (w > kMaxDecodeCtas) w = kMaxDecodeCtas;
+    if (a.decode_ctas > 0 && a.decode_ctas < w) w = a.decode_ctas;
+    return w;
+}
+
+// Launch size: whole waves, enough that no CTA's share exceeds kIdCap blocks for the
+// largest decode work these arguments allow (every request a decode row at the maximum
+// context); capped at kMaxDecodeCtas (the kernel flags a step that would need more).
+int decode_grid(const StepArgs& a, int wave) {
+    const long long per_req = ((long long)a.max_context_len + 1 + kBlockSize - 1) / kBlockSize;
+    const long long p_upper = per_req * (long long)a.num_reqs;
+    const long long per_launch_wave = (long long)wave * kIdCap;
+    long long waves = (p_upper + per_launch_wave - 1) / per_launch_wave;
+    if (waves < 1) waves = 1;
+    const long long max_waves = kMaxDecodeCtas / wave;
+    if (waves > max_waves) waves = max_waves > 0 ? max_waves : 1;
+    return (int)(waves * wave);
 }
 
 }  // namespace
@@ -457,11 +504,12 @@ int decode_grid(const StepArgs& a) {
 cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream) {
     const StepLayout& L = a.lay;
     const size_t smem = sizeof(DecodeSmem) + 128;
-    return launch_pdl(decode_kernel, dim3(decode_grid(a)), dim3(kDecThreads), smem, stream,
+    const int wave = decode_wave(a);
+    return launch_pdl(decode_kernel, dim3(decode_grid(a, wave)), dim3(kDecThreads), smem, stream,
                       static_cast<const __nv_bfloat16*>(a.q), static_cast<__nv_bfloat16*>(a.out), a.cu_seqlens_q,
                       a.context_lens, a.block_tables, a.max_blocks_per_seq, a.num_blocks,
                       static_cast<const uint8_t*>(a.k_cache), static_cast<const uint8_t*>(a.v_cache),
-                      reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs,
+                      reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs, wave,
                       reinterpret_cast<float*>(a.ws + L.part_acc_off), reinterpret_cast<float2*>(a.ws + L.part_ml_off),
                       reinterpret_cast<int32_t*>(a.ws + L.seg_count_off), a.softmax_scale * 1.4426950408889634f, a.err);
 }

@@ -184,9 +184,12 @@ KVP_API kvp_status paged_attention_step(kvp_pool* pool, const void* q, void* out
                                 size_t workspace_bytes, kvp_stream stream);
 
 /* Decode split: the 16-token blocks of all decode rows of a step are shared out evenly,
- * in request order, among `ctas` CTAs (0 = one per SM, the default; at most 1024); a
- * row whose blocks fall to several CTAs is finished by a merge of their partial results.
- * The workspace size does not depend on this setting.  Host-only. */
+ * in request order, among `ctas` CTAs at a time (0 = one per SM, the default; at most
+ * 1024); a CTA takes at most 2,048 blocks, so a step with more than ctas x 2,048 decode
+ * blocks runs in several waves of CTAs (at most 1024 CTAs in all: a step whose decode rows
+ * hold more blocks than that allows sets KVP_ERRBIT_BAD_META).  A row whose blocks fall to
+ * several CTAs is finished by a merge of their partial results.  The workspace size does
+ * not depend on this setting.  Host-only. */
 KVP_API kvp_status kv_pool_set_decode_ctas(kvp_pool* pool, int ctas);
 
 /* Synchronise `stream`, then read and clear the pool's device error word.  *bits (may be
