@@ -195,7 +195,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
     const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out, const int32_t* __restrict__ cu,
     const int32_t* __restrict__ ctx, const int32_t* __restrict__ tables, int max_blocks, int num_blocks,
     const uint8_t* __restrict__ k_cache, const uint8_t* __restrict__ v_cache, const int32_t* __restrict__ page_off,
-    int num_reqs, int wave, float* __restrict__ part_acc, float2* __restrict__ part_ml,
+    int num_reqs, int wave, const int32_t* __restrict__ counters, float* __restrict__ part_acc,
+    float2* __restrict__ part_ml,
     int32_t* __restrict__ seg_count, float scale_log2, uint32_t* __restrict__ err) {
     extern __shared__ uint8_t smem_raw[];
     DecodeSmem& S = *reinterpret_cast<DecodeSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -204,7 +205,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
     grid_dep_launch();
     const int P = page_off[num_reqs];
     if (P <= 0) return;
-    const int G = decode_ctas_used(P, wave, gridDim.x);
+    // SMs left to this step's prefill tiles run them meanwhile (unless the launch is too
+    // small for the narrower waves that would need)
+    int G = decode_ctas_used(P, max(1, min(wave, counters[2])), gridDim.x);
+    if (G == 0) G = decode_ctas_used(P, wave, gridDim.x);
     if (G == 0) {
         // the launch has too few CTAs for this many blocks (the host sizes it from an
         // upper bound, so this means inconsistent metadata)
@@ -510,6 +514,7 @@ cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream) {
                       a.context_lens, a.block_tables, a.max_blocks_per_seq, a.num_blocks,
                       static_cast<const uint8_t*>(a.k_cache), static_cast<const uint8_t*>(a.v_cache),
                       reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs, wave,
+                      reinterpret_cast<const int32_t*>(a.ws + L.counters_off),
                       reinterpret_cast<float*>(a.ws + L.part_acc_off), reinterpret_cast<float2*>(a.ws + L.part_ml_off),
                       reinterpret_cast<int32_t*>(a.ws + L.seg_count_off), a.softmax_scale * 1.4426950408889634f, a.err);
 }

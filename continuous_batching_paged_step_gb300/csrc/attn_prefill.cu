@@ -64,6 +64,7 @@ struct __align__(1024) PrefillSmem {
 
 struct PrefillArgs {
     const int32_t* counters;
+    int32_t* done;               // CTAs that have finished (zeroed by the metadata kernel)
     const int4* tiles;
     const int32_t* cu;
     const int32_t* ctx;
@@ -203,19 +204,13 @@ __device__ __forceinline__ void softmax_tile(PrefillSmem& S, const PrefillArgs& 
     }
 }
 
-__global__ void __launch_bounds__(kPreThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                   const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    PrefillSmem& S =
-        *reinterpret_cast<PrefillSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tile = blockIdx.x, g = blockIdx.y;
-    grid_dep_wait();     // work list, cache contents
-    grid_dep_launch();
-    if (tile >= a.counters[1]) return;
+__device__ __forceinline__ void prefill_cta(const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                                            const CUtensorMap& tmap_v, const PrefillArgs& a, PrefillSmem& S, int tile,
+                                            int g) {
+    if (tile >= __ldcg(&a.counters[1])) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int4 td = a.tiles[tile];
+    const int4 td = __ldcg(&a.tiles[tile]);
     const int r = td.x, tok0 = td.y, ntok = td.z;
     const int ctx_r = a.ctx[r];
     const int q_len = a.cu[r + 1] - a.cu[r];
@@ -392,6 +387,26 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     }
 }
 
+// Launched right after the decode kernel, as its programmatic dependent: CTAs start as
+// soon as every decode CTA has passed its own wait for the step's metadata kernel (so the
+// work list and the appended K/V are complete) and take the SMs the decode leaves free.
+// The grid finishes only after the decode grid has: its last CTA to leave waits for it.
+__global__ void __launch_bounds__(kPreThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    PrefillSmem& S =
+        *reinterpret_cast<PrefillSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    grid_dep_launch();
+    // blockIdx.x = KV head, blockIdx.y = tile: CTAs start in work-list order (longest first)
+    prefill_cta(tmap_q, tmap_k, tmap_v, a, S, blockIdx.y, blockIdx.x);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int total = gridDim.x * gridDim.y;
+        if (atomicAdd(a.done, 1) == total - 1) grid_dep_wait();
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_prefill(const StepArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
@@ -400,6 +415,7 @@ cudaError_t launch_prefill(const StepArgs& a, const CUtensorMap* tmap_q, const C
     if (L.max_prefill_tiles <= 0 || a.max_q_len < 2) return cudaSuccess;
     PrefillArgs pa;
     pa.counters = reinterpret_cast<const int32_t*>(a.ws + L.counters_off);
+    pa.done = reinterpret_cast<int32_t*>(a.ws + L.counters_off) + 3;
     pa.tiles = reinterpret_cast<const int4*>(a.ws + L.prefill_tiles_off);
     pa.cu = a.cu_seqlens_q;
     pa.ctx = a.context_lens;
@@ -409,7 +425,7 @@ cudaError_t launch_prefill(const StepArgs& a, const CUtensorMap* tmap_q, const C
     pa.out = static_cast<__nv_bfloat16*>(a.out);
     pa.err = a.err;
     pa.scale_log2 = a.softmax_scale * 1.4426950408889634f;
-    dim3 grid(L.max_prefill_tiles, kNumKvHeads);
+    dim3 grid(kNumKvHeads, L.max_prefill_tiles);
     const size_t smem = sizeof(PrefillSmem) + 1024;
     return launch_pdl(prefill_kernel, grid, dim3(kPreThreads), smem, stream, *tmap_q, *tmap_k, *tmap_v, pa);
 }

@@ -12,6 +12,11 @@
 //   q_r >= 2 (prefill chunk): one tile per 64 query tokens (two MMA tiles of 32 tokens x
 //     4 query heads of a KV group), emitted last tile first so the longest tiles start
 //     earliest.
+// SM split: the decode rows are HBM-bound and the prefill tiles tensor-bound, so the
+// attention kernels run side by side: the decode kernel takes counters[2] CTAs (one per
+// SM) and leaves the other SMs to prefill tiles, which start while the decode runs.  The
+// split follows a simple cost model (below) of the two kernels' work; counters[3] is the
+// prefill kernel's exit count, zeroed here.
 // One CTA of 1024 threads scans the requests in rounds of 1024 (block-wide exclusive
 // scan).  Inconsistent metadata sets KVP_ERRBIT_BAD_META; a request that fails its own
 // checks gets no work, and a cu_seqlens array that is not a monotone map of
@@ -24,6 +29,25 @@ namespace kvp {
 namespace {
 
 constexpr int kPrepThreads = 1024;
+
+// Cost model of the SM split, in units of one key tile of one prefill CTA (128 keys x
+// 64 query tokens x 4 heads through QK^T, softmax and P.V: about 2.2 us on a GB300 SM).
+// A prefill CTA costs its key tiles plus a fixed start/finish; one decode block (64 KiB of
+// K and V) costs a decode CTA about 0.68 units.  Both kinds of work are bound by their
+// SM's own throughput (tensor pipe / issue), so the SMs are shared out in proportion to
+// each side's SM-time, biased a little towards the decode: the prefill can spread over
+// every SM once the decode is done, but a late decode CTA cannot be helped.
+constexpr float kTileFixedUnits = 2.f;
+constexpr float kDecodeUnitsPerBlock = 0.68f;
+constexpr float kPrefillShareBias = 0.92f;
+
+// Decode CTAs for P decode blocks next to prefill work w (units) on n SMs.
+__device__ int decode_sm_share(int P, float w, int n) {
+    if (P <= 0 || w <= 0.f || n < 2) return n;
+    const float d = P * kDecodeUnitsPerBlock;
+    const int s = (int)(n * kPrefillShareBias * w / (w + d));
+    return max(1, min(n, n - s));
+}
 
 __device__ __forceinline__ int2 warp_incl_scan(int2 v, int lane) {
 #pragma unroll
@@ -40,12 +64,13 @@ __device__ __forceinline__ int2 warp_incl_scan(int2 v, int lane) {
 
 __global__ void __launch_bounds__(kPrepThreads) step_prep_kernel(
     const int32_t* __restrict__ cu, const int32_t* __restrict__ ctx, int num_reqs, int num_tokens, int max_q_len,
-    int max_context_len, int max_blocks, int max_prefill_tiles, int32_t* __restrict__ counters,
+    int max_context_len, int max_blocks, int max_prefill_tiles, int num_sms, int32_t* __restrict__ counters,
     int32_t* __restrict__ page_off, int32_t* __restrict__ seg_count, int4* __restrict__ pre_tiles,
     uint32_t* __restrict__ err) {
     __shared__ int s_ok;
     __shared__ int2 s_warp[32];
     __shared__ int2 s_base;
+    __shared__ float s_w[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     grid_dep_launch();
     if (tid == 0) {
@@ -58,6 +83,7 @@ __global__ void __launch_bounds__(kPrepThreads) step_prep_kernel(
     __syncthreads();
     const bool all_ok = s_ok != 0;
     if (!all_ok && tid == 0) raise_error(err, kErrBadMeta);
+    float w_units = 0.f;   // this thread's prefill work
     for (int round = 0; round < num_reqs; round += kPrepThreads) {
         const int r = round + tid;
         int2 n = make_int2(0, 0);   // x: decode blocks, y: prefill tiles
@@ -73,6 +99,11 @@ __global__ void __launch_bounds__(kPrepThreads) step_prep_kernel(
                 n.x = (c + 1 + kBlockSize - 1) / kBlockSize;
             } else if (q > 1) {
                 n.y = (q + kPrefillTileTokens - 1) / kPrefillTileTokens;
+                for (int t = 0; t < n.y; ++t) {
+                    const int end = c + min(q, (t + 1) * kPrefillTileTokens);   // keys of the tile's last row
+                    const float u = (float)((end + 127) / 128) + kTileFixedUnits;
+                    w_units += u;
+                }
             }
         }
         const int2 incl = warp_incl_scan(n, lane);
@@ -106,10 +137,18 @@ __global__ void __launch_bounds__(kPrepThreads) step_prep_kernel(
         if (tid == kPrepThreads - 1) s_base = make_int2(dx + n.x, dz + n.y);
         __syncthreads();
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) w_units += __shfl_xor_sync(0xffffffffu, w_units, o);
+    if (lane == 0) s_w[warp] = w_units;
+    __syncthreads();
     if (tid == 0) {
         const int2 b = s_base;
+        float w = 0.f;
+        for (int i = 0; i < kPrepThreads / 32; ++i) w += s_w[i];
         page_off[num_reqs] = b.x;
         counters[1] = min(b.y, max_prefill_tiles);
+        counters[2] = decode_sm_share(b.x, w * kNumKvHeads, num_sms);
+        counters[3] = 0;
     }
     // This kernel reads nothing the previous one (kv_append) writes, so it ran alongside
     // it; it finishes only after that kernel has, so that later kernels, which wait for
@@ -146,7 +185,8 @@ cudaError_t launch_step_prep(const StepArgs& a, cudaStream_t stream) {
     const StepLayout& L = a.lay;
     return launch_pdl(step_prep_kernel, dim3(1), dim3(kPrepThreads), 0, stream, a.cu_seqlens_q, a.context_lens,
                       a.num_reqs, a.num_tokens, a.max_q_len, a.max_context_len, a.max_blocks_per_seq,
-                      L.max_prefill_tiles, reinterpret_cast<int32_t*>(a.ws + L.counters_off),
+                      L.max_prefill_tiles, a.num_sms > 0 ? a.num_sms : 1,
+                      reinterpret_cast<int32_t*>(a.ws + L.counters_off),
                       reinterpret_cast<int32_t*>(a.ws + L.page_off_off),
                       reinterpret_cast<int32_t*>(a.ws + L.seg_count_off),
                       reinterpret_cast<int4*>(a.ws + L.prefill_tiles_off), a.err);

@@ -375,6 +375,10 @@ kvp_status paged_attention_step(kvp_pool* p, const void* q, void* out, const int
     a.decode_ctas = p->decode_ctas;
     if (timed_launch(p, KVP_KERNEL_PREP, s, [&] { return kvp::launch_step_prep(a, s); }) != cudaSuccess)
         return KVP_E_CUDA;
+    // decode first; the prefill kernel follows as its programmatic dependent and runs on
+    // the SMs the decode leaves free (the metadata kernel sizes the split)
+    if (timed_launch(p, KVP_KERNEL_DECODE, s, [&] { return kvp::launch_decode(a, s); }) != cudaSuccess)
+        return KVP_E_CUDA;
     if (max_q_len >= 2 && lay.max_prefill_tiles > 0) {
         CUtensorMap tq;
         if (!encode_q_map(&tq, q, num_tokens)) return KVP_E_CUDA;
@@ -382,8 +386,6 @@ kvp_status paged_attention_step(kvp_pool* p, const void* q, void* out, const int
                          [&] { return kvp::launch_prefill(a, &tq, &p->tmap_k, &p->tmap_v, s); }) != cudaSuccess)
             return KVP_E_CUDA;
     }
-    if (timed_launch(p, KVP_KERNEL_DECODE, s, [&] { return kvp::launch_decode(a, s); }) != cudaSuccess)
-        return KVP_E_CUDA;
     return KVP_OK;
 }
 

@@ -17,7 +17,7 @@ namespace kvp {
 struct StepLayout {
     int max_prefill_tiles;   // (request, 32-token q tile) work items of prefill chunks
     int max_partials;        // split-KV partial slots: request r cut by CTA c uses r + c
-    size_t counters_off;     // int32[8]: 1 = prefill tiles
+    size_t counters_off;     // int32[8]: 1 = prefill tiles, 2 = decode CTAs, 3 = prefill CTAs done
     size_t page_off_off;     // int32 [num_reqs + 1]: first global decode block of each request
     size_t seg_count_off;    // int32 [num_reqs]: CTAs done with their part of a split decode row
     size_t prefill_tiles_off;// int4 {r, first token of tile, tokens in tile, 0}
