@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <cstring>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include "kvpaged.h"
@@ -190,6 +191,57 @@ cudaError_t timed_launch(kvp_pool* p, int kind, cudaStream_t s, F&& fn) {
     return cudaSuccess;
 }
 
+// Device address of page-locked host memory (cudaHostAlloc / cudaHostRegister), or
+// false for any other pointer.
+bool host_device_ptr(const void* h, void** d) {
+    cudaPointerAttributes at;
+    if (!h || cudaPointerGetAttributes(&at, h) != cudaSuccess) {
+        cudaGetLastError();   // clear the sticky-free error of a failed query
+        return false;
+    }
+    if (at.type != cudaMemoryTypeHost || !at.devicePointer) return false;
+    *d = at.devicePointer;
+    return aligned16(*d);
+}
+
+// Copy n whole blocks (K and V) in launches of up to kMoveChunk: a side with ids is a pool
+// indexed by block id, a side without is a host buffer indexed by list position.
+kvp_status move_blocks(kvp_pool* p, const void* src_k, const void* src_v, const int32_t* src_ids, void* dst_k,
+                       void* dst_v, const int32_t* dst_ids, int n, cudaStream_t s) {
+    static thread_local kvp::BlockMoveArgs a;   // 8 KiB of ids: kept off the stack
+    for (int off = 0; off < n; off += kvp::kMoveChunk) {
+        const int m = std::min(kvp::kMoveChunk, n - off);
+        const size_t host_off = (size_t)off * kvp::kBlockBytes;
+        a.n = m;
+        a.src[0] = static_cast<const uint8_t*>(src_k) + (src_ids ? 0 : host_off);
+        a.src[1] = static_cast<const uint8_t*>(src_v) + (src_ids ? 0 : host_off);
+        a.dst[0] = static_cast<uint8_t*>(dst_k) + (dst_ids ? 0 : host_off);
+        a.dst[1] = static_cast<uint8_t*>(dst_v) + (dst_ids ? 0 : host_off);
+        a.src_ids_used = src_ids ? 1 : 0;
+        a.dst_ids_used = dst_ids ? 1 : 0;
+        if (src_ids) std::memcpy(a.src_ids, src_ids + off, (size_t)m * sizeof(int32_t));
+        if (dst_ids) std::memcpy(a.dst_ids, dst_ids + off, (size_t)m * sizeof(int32_t));
+        if (timed_launch(p, KVP_KERNEL_BLOCKS, s, [&] { return kvp::launch_block_move(a, s); }) != cudaSuccess)
+            return KVP_E_CUDA;
+    }
+    return KVP_OK;
+}
+
+// The checks of kv_block_free: every id in range, no refcount driven below zero.
+kvp_status check_release(const kvp_pool* p, int n, const int32_t* ids) {
+    std::vector<int32_t> sorted(ids, ids + n);
+    std::sort(sorted.begin(), sorted.end());
+    for (int i = 0; i < n;) {
+        const int32_t id = sorted[i];
+        if (id < 0 || id >= p->num_blocks) return KVP_E_BAD_BLOCK;
+        int k = i;
+        while (k < n && sorted[k] == id) ++k;
+        if (p->refcnt[id] < k - i) return KVP_E_REFCOUNT;
+        i = k;
+    }
+    return KVP_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -277,16 +329,8 @@ kvp_status kv_block_ref(kvp_pool* p, int n, const int32_t* ids) {
 
 kvp_status kv_block_free(kvp_pool* p, int n, const int32_t* ids) {
     if (!p || n < 0 || (n > 0 && !ids)) return KVP_E_INVALID_ARG;
-    std::vector<int32_t> sorted(ids, ids + n);
-    std::sort(sorted.begin(), sorted.end());
-    for (int i = 0; i < n;) {
-        const int32_t id = sorted[i];
-        if (id < 0 || id >= p->num_blocks) return KVP_E_BAD_BLOCK;
-        int k = i;
-        while (k < n && sorted[k] == id) ++k;
-        if (p->refcnt[id] < k - i) return KVP_E_REFCOUNT;  // would go below zero
-        i = k;
-    }
+    const kvp_status st = check_release(p, n, ids);
+    if (st != KVP_OK) return st;
     for (int i = 0; i < n; ++i) {
         const int32_t id = ids[i];
         if (--p->refcnt[id] == 0) {
@@ -296,6 +340,79 @@ kvp_status kv_block_free(kvp_pool* p, int n, const int32_t* ids) {
         mark_dirty(p, id);
     }
     return KVP_OK;
+}
+
+kvp_status kv_block_cow(kvp_pool* p, int n, const int32_t* src_ids, int32_t* out_ids, kvp_stream stream) {
+    if (!p || n < 0 || (n > 0 && (!src_ids || !out_ids))) return KVP_E_INVALID_ARG;
+    // decide every copy first (a block listed twice is shared by one fewer reference the
+    // second time), so that nothing changes when a check fails
+    std::unordered_map<int32_t, int> taken;
+    std::vector<char> copy(n, 0);
+    int copies = 0;
+    for (int i = 0; i < n; ++i) {
+        const int32_t id = src_ids[i];
+        if (id < 0 || id >= p->num_blocks || p->refcnt[id] <= 0) return KVP_E_BAD_BLOCK;
+        int& t = taken[id];
+        if (p->refcnt[id] - t > 1) {
+            copy[i] = 1;
+            ++t;
+            ++copies;
+        }
+    }
+    if ((size_t)copies > p->free_list.size()) return KVP_E_NO_BLOCKS;
+    if (copies > 0) {
+        const kvp_status st = ensure_device(p);
+        if (st != KVP_OK) return st;
+    }
+    std::vector<int32_t> srcs, dsts;
+    srcs.reserve(copies);
+    dsts.reserve(copies);
+    for (int i = 0; i < n; ++i) {
+        const int32_t id = src_ids[i];
+        if (!copy[i]) {
+            out_ids[i] = id;
+            continue;
+        }
+        const int32_t nb = p->free_list.back();
+        p->free_list.pop_back();
+        p->free_pos[nb] = -1;
+        p->refcnt[nb] = 1;
+        p->refcnt[id] -= 1;
+        mark_dirty(p, nb);
+        mark_dirty(p, id);
+        out_ids[i] = nb;
+        srcs.push_back(id);
+        dsts.push_back(nb);
+    }
+    return move_blocks(p, p->k_cache, p->v_cache, srcs.data(), p->k_cache, p->v_cache, dsts.data(), copies,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+kvp_status kv_blocks_swap_out(kvp_pool* p, int n, const int32_t* ids, void* host_k, void* host_v,
+                              kvp_stream stream) {
+    if (!p || n < 0 || (n > 0 && !ids)) return KVP_E_INVALID_ARG;
+    if (n == 0) return KVP_OK;
+    kvp_status st = check_release(p, n, ids);
+    if (st != KVP_OK) return st;
+    void *dk = nullptr, *dv = nullptr;
+    if (!host_device_ptr(host_k, &dk) || !host_device_ptr(host_v, &dv)) return KVP_E_INVALID_ARG;
+    if ((st = ensure_device(p)) != KVP_OK) return st;
+    st = move_blocks(p, p->k_cache, p->v_cache, ids, dk, dv, nullptr, n, reinterpret_cast<cudaStream_t>(stream));
+    if (st != KVP_OK) return st;
+    return kv_block_free(p, n, ids);
+}
+
+kvp_status kv_blocks_swap_in(kvp_pool* p, int n, const void* host_k, const void* host_v, int32_t* out_ids,
+                             kvp_stream stream) {
+    if (!p || n < 0 || (n > 0 && !out_ids)) return KVP_E_INVALID_ARG;
+    if (n == 0) return KVP_OK;
+    if ((size_t)n > p->free_list.size()) return KVP_E_NO_BLOCKS;
+    void *dk = nullptr, *dv = nullptr;
+    if (!host_device_ptr(host_k, &dk) || !host_device_ptr(host_v, &dv)) return KVP_E_INVALID_ARG;
+    kvp_status st = ensure_device(p);
+    if (st != KVP_OK) return st;
+    if ((st = kv_block_alloc(p, n, out_ids)) != KVP_OK) return st;
+    return move_blocks(p, dk, dv, nullptr, p->k_cache, p->v_cache, out_ids, n, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kv_pool_num_free(const kvp_pool* p) { return p ? (int)p->free_list.size() : -1; }

@@ -63,6 +63,21 @@ cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const StepArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
                            const CUtensorMap* tmap_v, cudaStream_t stream);
 
+// Whole-block copies (K and V, 32 KiB each): block i of the launch reads
+// src[kv] + (src_ids_used ? src_ids[i] : i) * 32 KiB and writes dst[kv] + (dst_ids_used ?
+// dst_ids[i] : i) * 32 KiB, for kv = 0 (K), 1 (V).  Pools are indexed by block id, host
+// buffers by position in the list.
+constexpr int kMoveChunk = 1024;
+struct BlockMoveArgs {
+    const uint8_t* src[2];
+    uint8_t* dst[2];
+    int n;
+    int src_ids_used, dst_ids_used;
+    int32_t src_ids[kMoveChunk];
+    int32_t dst_ids[kMoveChunk];
+};
+cudaError_t launch_block_move(const BlockMoveArgs& a, cudaStream_t stream);
+
 // Launch `kernel` so that it may start while the previous kernel of `stream` finishes
 // (programmatic dependent launch); the kernel must call grid_dep_wait() before it reads
 // what earlier kernels wrote.

@@ -45,8 +45,12 @@ SIGNATURES = {
     "paged_attention_step_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "paged_attention_noalloc_capacity": (_SZ, []),
     "kvp_selftest_bounded_wait": (_I, [ctypes.c_longlong, _P]),
+    "kv_block_cow": (_I, [_P, _I, _I32P, _I32P, _P]),
+    "kv_blocks_swap_out": (_I, [_P, _I, _I32P, _P, _P, _P]),
+    "kv_blocks_swap_in": (_I, [_P, _I, _P, _P, _I32P, _P]),
 }
-KERNEL_NAMES = ("kv_append", "step_prep", "prefill_tcgen05", "decode_splitkv")
+KERNEL_NAMES = ("kv_append", "step_prep", "prefill_tcgen05", "decode_splitkv", "block_move")
+BLOCK_BYTES = N_KV_HEADS * BLOCK_SIZE * HEAD_DIM * 2   # one block of K (or of V): 32 KiB
 
 
 class KVPError(RuntimeError):
@@ -144,6 +148,52 @@ def kv_block_ref(pool: int, ids):
 def kv_block_free(pool: int, ids):
     a, p = _ids(ids)
     _check(lib.kv_block_free(pool, a.size, p), "kv_block_free")
+
+
+def _stream_or_null(stream):
+    """The stream handle, or None (the legacy default stream) when torch has no CUDA."""
+    if stream is not None:
+        return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    import torch
+    return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+
+
+def kv_block_cow(pool: int, src_ids, stream=None) -> np.ndarray:
+    """Copy-on-write: for each listed block, the block itself if its refcount is 1, else a
+    new block holding a copy of it (the source loses one reference)."""
+    a, p = _ids(src_ids)
+    out = np.empty(a.size, dtype=np.int32)
+    _check(lib.kv_block_cow(pool, a.size, p, out.ctypes.data_as(_I32P), _stream_or_null(stream)), "kv_block_cow")
+    return out
+
+
+def _pinned(t, n: int, what: str):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous pinned host tensor")
+    if t.numel() * t.element_size() < n * BLOCK_BYTES:
+        raise ValueError(f"{what} holds fewer than {n} blocks")
+
+
+def kv_blocks_swap_out(pool: int, ids, host_k, host_v, stream=None):
+    """Copy the listed blocks' K and V to pinned host tensors (block i at byte i * 32 KiB)
+    and release one reference of each."""
+    a, p = _ids(ids)
+    _pinned(host_k, a.size, "host_k")
+    _pinned(host_v, a.size, "host_v")
+    _check(lib.kv_blocks_swap_out(pool, a.size, p, _ptr(host_k), _ptr(host_v), _stream(stream)),
+           "kv_blocks_swap_out")
+
+
+def kv_blocks_swap_in(pool: int, host_k, host_v, n: int, stream=None) -> np.ndarray:
+    """Allocate n blocks and copy block i of the pinned host tensors into them; returns
+    the new block ids."""
+    _pinned(host_k, n, "host_k")
+    _pinned(host_v, n, "host_v")
+    out = np.empty(n, dtype=np.int32)
+    _check(lib.kv_blocks_swap_in(pool, n, _ptr(host_k), _ptr(host_v), out.ctypes.data_as(_I32P), _stream(stream)),
+           "kv_blocks_swap_in")
+    return out
 
 
 def kv_pool_num_free(pool: int) -> int:

@@ -128,6 +128,46 @@ KVP_API kvp_status kv_block_ref(kvp_pool* pool, int n, const int32_t* ids);
  * scheduling").  KVP_E_REFCOUNT if a block would go below 0 (double free). */
 KVP_API kvp_status kv_block_free(kvp_pool* pool, int n, const int32_t* ids);
 
+/* Copy-on-write (page "11.2", section 11.2.3, the paragraph on sharing: output sequences
+ * of one request that share the prompt's last, partly filled block copy it before one of
+ * them writes a new token into it; page "连续批处理与 PagedAttention 原理", section
+ * "块管理器": copy-on-write is one of the block manager's operations).  For each listed
+ * block, in order: if its refcount is 1, out_ids[i] = src_ids[i] and nothing changes;
+ * if it is shared, a free block is allocated (refcount := 1), the source's K and V
+ * (32 KiB each) are copied into it on `stream`, the source's refcount drops by 1 and
+ * out_ids[i] is the new block.  The caller then points its block table at out_ids[i]
+ * before writing (kv_append refuses writes into shared blocks).  src_ids / out_ids are
+ * host arrays of n.  All-or-nothing on the host: KVP_E_BAD_BLOCK for an id out of range
+ * or free, KVP_E_NO_BLOCKS if the free list cannot supply the copies; KVP_E_CUDA if a
+ * launch fails (the allocations stand; the copies may be missing).  Launches nothing
+ * when no listed block is shared. */
+KVP_API kvp_status kv_block_cow(kvp_pool* pool, int n, const int32_t* src_ids, int32_t* out_ids,
+                                kvp_stream stream);
+
+/* Swap out (page "Continuous Batching 深入实现", section "第四层：Preemption 与 Recompute
+ * vs Swap": a preempted request's KV is copied from HBM to host memory and its GPU
+ * blocks are released; page "连续批处理与 PagedAttention 原理", section "抢占策略").
+ * Block ids[i]'s K and V go to host_k + i * 32 KiB and host_v + i * 32 KiB, then one
+ * reference of each listed block is released (as kv_block_free).  host_k / host_v: page-
+ * locked host memory (cudaHostAlloc / cudaHostRegister) of at least n * 32 KiB, written
+ * by a kernel on `stream`; they hold the data once the stream has passed this call.  The
+ * released blocks may be handed out again at once: later writes to them must be ordered
+ * after this call (same stream, or after synchronising it).  KVP_E_BAD_BLOCK /
+ * KVP_E_REFCOUNT as kv_block_free, KVP_E_INVALID_ARG if a host buffer is not page-locked
+ * memory the device can reach (nothing changes then). */
+KVP_API kvp_status kv_blocks_swap_out(kvp_pool* pool, int n, const int32_t* ids, void* host_k,
+                                      void* host_v, kvp_stream stream);
+
+/* Swap in (same passages: the KV is copied back when the request resumes): allocate n
+ * blocks (refcount := 1) into out_ids[n] (host) and copy host_k + i * 32 KiB /
+ * host_v + i * 32 KiB into block out_ids[i] on `stream` (page-locked host memory as for
+ * kv_blocks_swap_out, which must stay unchanged until the stream has passed this call).
+ * The caller writes out_ids into the request's block table.  KVP_E_NO_BLOCKS if fewer
+ * than n blocks are free, KVP_E_INVALID_ARG for host buffers the device cannot reach
+ * (nothing changes then). */
+KVP_API kvp_status kv_blocks_swap_in(kvp_pool* pool, int n, const void* host_k, const void* host_v,
+                                     int32_t* out_ids, kvp_stream stream);
+
 /* Number of free blocks, or -1 for NULL. */
 KVP_API int kv_pool_num_free(const kvp_pool* pool);
 
@@ -225,9 +265,10 @@ KVP_API size_t paged_attention_noalloc_capacity(void);
 
 /* ------------------------------------------------------------------ diagnostics ----
  * Per-kernel timing of the library's own launches, for benchmarks.  After
- * kv_pool_enable_timing(pool, max_launches) every kernel launch of kv_append and
- * paged_attention_step (on this pool's device) is bracketed by two CUDA events on the
- * launching stream, up to max_launches launches (0 disables and frees the events).
+ * kv_pool_enable_timing(pool, max_launches) every kernel launch of kv_append,
+ * paged_attention_step and the block copies (on this pool's device) is bracketed by two
+ * CUDA events on the launching stream, up to max_launches launches (0 disables and frees
+ * the events).
  * kv_pool_read_timing waits for the last recorded event, writes the number of timed
  * launches and the summed milliseconds of each kernel kind into counts[KVP_NUM_KERNELS]
  * and ms[KVP_NUM_KERNELS], and restarts the record. */
@@ -235,7 +276,8 @@ KVP_API size_t paged_attention_noalloc_capacity(void);
 #define KVP_KERNEL_PREP    1
 #define KVP_KERNEL_PREFILL 2
 #define KVP_KERNEL_DECODE  3   /* split-KV partials are merged inside this kernel */
-#define KVP_NUM_KERNELS    4
+#define KVP_KERNEL_BLOCKS  4   /* block copies of kv_block_cow / kv_blocks_swap_* */
+#define KVP_NUM_KERNELS    5
 KVP_API kvp_status kv_pool_enable_timing(kvp_pool* pool, int max_launches);
 KVP_API kvp_status kv_pool_read_timing(kvp_pool* pool, int* counts, float* ms);
 

@@ -161,3 +161,40 @@ def test_workspace_size_and_split_setting(kp):
 def test_status_strings(kp):
     for code in kp.STATUS_NAMES:
         assert kp.lib.kvp_status_string(code)
+
+
+def test_cow_and_swap_host_checks(kp):
+    """The host-side rules of copy-on-write and swap (nothing here reaches a device)."""
+    h = kp.kv_pool_create(FAKE_K, FAKE_V, num_blocks=8)
+    try:
+        a = [int(b) for b in kp.kv_block_alloc(h, 6)]
+        # blocks nobody shares come back as they are, with nothing launched
+        assert kp.kv_block_cow(h, a[:3]).tolist() == a[:3]
+        assert [kp.kv_block_refcount(h, b) for b in a[:3]] == [1, 1, 1]
+        # free or out-of-range sources
+        free = [b for b in range(8) if b not in a]
+        for bad in ([free[0]], [8], [-1]):
+            with pytest.raises(kp.KVPError) as e:
+                kp.kv_block_cow(h, bad)
+            assert e.value.status == -3
+        # three copies needed, two free blocks: refused, nothing changes
+        kp.kv_block_ref(h, [a[0], a[1], a[2]])
+        with pytest.raises(kp.KVPError) as e:
+            kp.kv_block_cow(h, [a[0], a[1], a[2]])
+        assert e.value.status == -2
+        assert kp.kv_pool_num_free(h) == 2 and [kp.kv_block_refcount(h, b) for b in a[:3]] == [2, 2, 2]
+        # swap: release checks first, then the host buffers must be page-locked memory
+        import torch
+        buf = torch.empty(4 * kp.BLOCK_BYTES, dtype=torch.uint8)       # pageable
+        with pytest.raises(ValueError):
+            kp.kv_blocks_swap_out(h, [a[3]], buf, buf)
+        st = kp.lib.kv_blocks_swap_out(h, 1, (ctypes.c_int32 * 1)(free[0]), buf.data_ptr(), buf.data_ptr(), None)
+        assert st == -7                                               # a free block
+        st = kp.lib.kv_blocks_swap_out(h, 1, (ctypes.c_int32 * 1)(a[3]), buf.data_ptr(), buf.data_ptr(), None)
+        assert st == -1 and kp.kv_block_refcount(h, a[3]) == 1         # pageable: refused, unchanged
+        out = (ctypes.c_int32 * 3)()
+        assert kp.lib.kv_blocks_swap_in(h, 3, buf.data_ptr(), buf.data_ptr(), out, None) == -2
+        assert kp.lib.kv_blocks_swap_in(h, 1, buf.data_ptr(), buf.data_ptr(), out, None) == -1
+        assert kp.kv_pool_num_free(h) == 2
+    finally:
+        kp.kv_pool_destroy(h)
