@@ -305,12 +305,7 @@ def run_gpu(a):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": round(total_ms / a.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": spec.name, "num_tokens": T, "num_reqs": spec.num_reqs,
-                   "decode_rows": sum(1 for q in spec.q_lens if q == 1),
-                   "prefill_chunks": [[q, c] for q, c in zip(spec.q_lens, spec.ctx_lens) if q > 1],
-                   "heads": "32 q / 8 kv, d 128", "block_size": 16, "kv_pool_blocks": spec.num_blocks,
-                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write outside the step events)",
-                   "parallelism": f"replicas x{world}"},
+        "config": step_config(spec, world),
         "decode_kv_gbs": rl_decode["achieved"] if rl_decode else None,
         "roofline": roofline, "roofline_secondary": secondary,
         "kernels_us": {k: round(v["avg_us"], 2) for k, v in kern.items()},
@@ -390,6 +385,16 @@ def run_e2e(a, step, stream, dev, flush, dist, world):
 
 # ---------------------------------------------------------------- reference arm
 
+def step_config(spec, world):
+    """The `config` object of a step workload's JSON line (both arms)."""
+    return {"workload": spec.name, "num_tokens": spec.num_tokens, "num_reqs": spec.num_reqs,
+            "decode_rows": sum(1 for q in spec.q_lens if q == 1),
+            "prefill_chunks": [[q, c] for q, c in zip(spec.q_lens, spec.ctx_lens) if q > 1],
+            "heads": "32 q / 8 kv, d 128", "block_size": 16, "kv_pool_blocks": spec.num_blocks,
+            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write outside the step events)",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(a):
     """The CPU oracle as it stands, on the same workload: each step is the oracle over a
     bounded sample of the step's rows, sized so the whole run takes a few minutes."""
@@ -417,7 +422,7 @@ def run_reference(a):
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(per * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": spec.name, "num_tokens": spec.num_tokens, "num_reqs": spec.num_reqs},
+            "config": step_config(spec, int(os.environ.get("WORLD_SIZE", "1"))),
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": workers, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
