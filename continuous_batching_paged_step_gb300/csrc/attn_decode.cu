@@ -66,8 +66,14 @@ struct __align__(128) DecodeSmem {
     uint32_t* err;
     uint64_t policy;
     uint64_t full[kDecStages];
-    uint64_t empty[kDecStages];
 };
+
+// atom.add with acquire-release ordering at CTA scope (shared memory).
+__device__ __forceinline__ unsigned atomic_add_acq_rel_cta(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
+    return old;
+}
 
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -146,19 +152,17 @@ __device__ __noinline__ void issue_block(DecodeSmem& S, int st, int q) {
     atomicMax(&S.issued, q + 1);
 }
 
-// Lane 0 of a warp that is done reading block `rel` (stage st, phase ph): the last of
-// the 16 warps refills the stage with block rel + kDecStages.
-__device__ __forceinline__ void release_stage(DecodeSmem& S, int st, uint32_t ph, int rel) {
-    mbar_arrive(&S.empty[st]);
-    const unsigned old = atomicAdd(&S.released[st], 1u);
+// Lane 0 of a warp that is done reading block `rel` (stage st; the warp's reads are
+// ordered before this by __syncwarp): the last of the 16 warps refills the stage with
+// block rel + kDecStages.  One shared atomic per warp and block: the count both elects
+// the refilling warp and orders every warp's reads (release) before the copy (acquire,
+// then a proxy fence for the bulk copy's write).
+__device__ __forceinline__ void release_stage(DecodeSmem& S, int st, int rel) {
+    const unsigned old = atomic_add_acq_rel_cta(&S.released[st], 1u);
     if ((old & (kDecWarps - 1)) != kDecWarps - 1) return;
     const int q = rel + kDecStages;
     if (q >= S.n_rel) return;
-    // every warp has arrived (or is about to): the wait only orders their reads before the copy
-    if (!mbar_wait(&S.empty[st], ph)) {
-        raise_error(S.err, kErrTimeout);
-        return;
-    }
+    fence_proxy_async_smem();
     issue_block(S, st, q);
 }
 
@@ -228,7 +232,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
     if (threadIdx.x == 0) {
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(&S.full[s], 1);
-            mbar_init(&S.empty[s], kDecWarps);
             S.released[s] = 0;
         }
         S.issued = 0;
@@ -380,7 +383,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
                         for (int t = 0; t < n_valid; ++t) pv_token(S.pbuf[warp][t], vt + t * kHeadBytes, lane, acc);
                     }
                     __syncwarp();
-                    if (lane == 0) release_stage(S, stage, phase, page - lo);
+                    if (lane == 0) release_stage(S, stage, page - lo);
                 }
             }
             if (++stage == kDecStages) {
