@@ -8,8 +8,10 @@
 //
 // * Balanced split: the 16-token blocks of all decode rows, concatenated in request
 //   order (page_off[r] = first global block of request r), are cut into equal contiguous
-//   ranges, one per CTA (one CTA per SM; fewer when there are under 4 blocks per CTA; more
-//   CTAs, in whole waves, when a range would exceed the 2,048 block ids a CTA stages).  A
+//   ranges, one per CTA (one CTA per SM of the decode's share of the SMs, which the step's
+//   metadata kernel sizes so that the prefill tiles run on the others; fewer CTAs when
+//   there are under 4 blocks per CTA; more, in whole waves, when a range would exceed the
+//   2,048 block ids a CTA stages).  A
 //   CTA walks its range request by request; a request cut by a range boundary produces one
 //   partial per CTA that touches it (slot r + cta), merged by whichever of those CTAs
 //   finishes last; a request inside one range is finished in place.

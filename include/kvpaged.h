@@ -215,7 +215,9 @@ KVP_API size_t paged_attention_workspace_size(const kvp_pool* pool, int num_reqs
  *   paged_attention_workspace_size(num_reqs, num_tokens, 32, max_context_len) bytes,
  *   scratch owned by the caller for the duration of the call (stream order).
  * Rows with q_len == 1 (decode) take the HBM-bound split-KV path; rows of requests with
- * q_len > 1 (prefill chunks) take the tcgen05 tensor-core path. */
+ * q_len > 1 (prefill chunks) take the tcgen05 tensor-core path.  The two kernels run side
+ * by side on disjoint SMs (the step's first kernel sizes the decode's share from the
+ * step's work); the call's work is complete, in stream order, when both are. */
 KVP_API kvp_status paged_attention_step(kvp_pool* pool, const void* q, void* out,
                                 const int32_t* cu_seqlens_q, const int32_t* context_lens,
                                 const int32_t* block_tables, int max_blocks_per_seq,
@@ -225,7 +227,8 @@ KVP_API kvp_status paged_attention_step(kvp_pool* pool, const void* q, void* out
 
 /* Decode split: the 16-token blocks of all decode rows of a step are shared out evenly,
  * in request order, among `ctas` CTAs at a time (0 = one per SM, the default; at most
- * 1024); a CTA takes at most 2,048 blocks, so a step with more than ctas x 2,048 decode
+ * 1024; a step that also has prefill chunks gives the decode at most the share of SMs its
+ * metadata kernel leaves it); a CTA takes at most 2,048 blocks, so a step with more than ctas x 2,048 decode
  * blocks runs in several waves of CTAs (at most 1024 CTAs in all: a step whose decode rows
  * hold more blocks than that allows sets KVP_ERRBIT_BAD_META).  A row whose blocks fall to
  * several CTAs is finished by a merge of their partial results.  The workspace size does
