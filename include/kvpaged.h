@@ -194,8 +194,8 @@ KVP_API kvp_status kv_append(kvp_pool* pool, const void* k_new, const void* v_ne
                      int num_reqs, int num_tokens, kvp_stream stream);
 
 /* --------------------------------------------------------- paged attention step ----
- * Workspace bytes paged_attention_step needs on this pool (it depends on the pool's
- * decode split) for a step with at most these sizes; 0 for bad arguments. */
+ * Workspace bytes paged_attention_step needs for a step with at most these sizes (the
+ * same for every pool and decode split); 0 for bad arguments. */
 KVP_API size_t paged_attention_workspace_size(const kvp_pool* pool, int num_reqs, int num_tokens,
                                       int n_q_heads, int max_context_len);
 
