@@ -5,74 +5,92 @@
 // offset p % 16.  The pool keeps each (block, KV head) tile of 16 x 128 bf16 contiguous,
 // so one (row, head) write is a single 256-byte run: 16 lanes each store 16 bytes.
 //
-// One CTA of 256 threads per packed row: the threads first look the row's request up in
-// cu_seqlens together (one round of loads instead of a serial binary search), then
-// threads 0..127 move K and 128..255 move V; within each half, thread t handles head
-// t / 16 and 16-byte chunk t % 16.  Loads of the new row are fully coalesced (2 KiB per
-// tensor per row); stores are 256-byte runs per head.
+// One warp per packed row (8 rows per CTA of 256 threads, so a whole step is one wave of
+// CTAs).  The CTA first copies cu_seqlens and context_lens into shared memory (steps of
+// up to 2,048 requests; larger ones search global memory); lane 0 of each warp then finds
+// its row's request by binary search (cu_seqlens is monotone), checks the context
+// length, the table entry and the block's refcount, and hands the
+// destination to the warp; the 32 lanes then move the row's 2 KiB of K and 2 KiB of V, 16
+// bytes each per pass, fully coalesced on the read side and in 256-byte runs per head
+// (half a warp) on the write side.
 #include "kvp_device.cuh"
 #include "kvp_launch.h"
 
 namespace kvp {
+
+constexpr int kAppendRowsPerCta = 8;   // one warp per row
+constexpr int kAppendSmemReqs = 2048;  // requests whose metadata a CTA stages in shared memory
 
 __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict__ k_new,
                                                         const uint4* __restrict__ v_new,
                                                         const int32_t* __restrict__ cu,
                                                         const int32_t* __restrict__ ctx,
                                                         const int32_t* __restrict__ tables, int max_blocks,
-                                                        int num_reqs, uint4* __restrict__ k_cache,
+                                                        int num_reqs, int num_tokens, uint4* __restrict__ k_cache,
                                                         uint4* __restrict__ v_cache,
                                                         const int32_t* __restrict__ refcnt, int num_blocks,
                                                         uint32_t* __restrict__ err) {
-    __shared__ long long s_dst;  // element-chunk index of (block, head 0, slot) or -1
-    __shared__ int s_req;
+    __shared__ int32_t s_cu[kAppendSmemReqs + 1];
+    __shared__ int32_t s_ctx[kAppendSmemReqs];
     grid_dep_launch();   // the step's metadata kernel does not read the pool
-    const int i = blockIdx.x;
-    if (threadIdx.x == 0) s_req = -1;
-    __syncthreads();
-    // request r with cu[r] <= i < cu[r+1]: all threads test requests in parallel
-    for (int r = threadIdx.x; r < num_reqs; r += blockDim.x)
-        if (cu[r] <= i && i < cu[r + 1]) s_req = r;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        long long dst = -1;
-        const int r = s_req;
-        if (r < 0) {
+    const bool staged = num_reqs <= kAppendSmemReqs;
+    if (staged) {
+        for (int k = threadIdx.x; k <= num_reqs; k += blockDim.x) s_cu[k] = cu[k];
+        for (int k = threadIdx.x; k < num_reqs; k += blockDim.x) s_ctx[k] = ctx[k];
+        __syncthreads();
+    }
+    const int32_t* cu_r = staged ? s_cu : cu;
+    const int32_t* ctx_r = staged ? s_ctx : ctx;
+    const int lane = threadIdx.x & 31;
+    const int i = blockIdx.x * kAppendRowsPerCta + (threadIdx.x >> 5);
+    if (i >= num_tokens) return;
+    long long dst = -1;   // element-chunk index of (block, head 0, slot), or -1
+    if (lane == 0) {
+        // the last request r with cu[r] <= i; the row belongs to it iff i < cu[r + 1]
+        int a = 0, b = num_reqs - 1;
+        while (a < b) {
+            const int mid = (a + b + 1) >> 1;
+            if (cu_r[mid] <= i) a = mid;
+            else b = mid - 1;
+        }
+        const int r = a;
+        if (!(cu_r[r] <= i && i < cu_r[r + 1])) {
             raise_error(err, kErrBadMeta);
         } else {
-            const int cl = ctx[r];
-            const long long p = (long long)cl + (i - cu[r]);
+            const int cl = ctx_r[r];
+            const long long p = (long long)cl + (i - cu_r[r]);
             const long long lb = p >> 4;
             if (cl < 0 || lb >= max_blocks) {
                 raise_error(err, kErrBadMeta);
             } else {
-                const int b = tables[(size_t)r * max_blocks + lb];
-                if (b < 0 || b >= num_blocks) {
+                const int bid = tables[(size_t)r * max_blocks + lb];
+                if (bid < 0 || bid >= num_blocks) {
                     raise_error(err, kErrBadBlock);
                 } else {
-                    const int rc = refcnt[b];
+                    const int rc = refcnt[bid];
                     if (rc == 1) {
-                        dst = ((long long)b * kNumKvHeads * kBlockSize + (p & 15)) * (kHeadBytes / 16);
+                        dst = ((long long)bid * kNumKvHeads * kBlockSize + (p & 15)) * (kHeadBytes / 16);
                     } else {
                         raise_error(err, rc == 0 ? kErrBadBlock : kErrSharedWrite);
                     }
                 }
             }
         }
-        s_dst = dst;
     }
-    __syncthreads();
-    const long long dst = s_dst;
+    dst = __shfl_sync(0xffffffffu, dst, 0);
     if (dst < 0) return;
-    const int t = threadIdx.x & 127;
-    const int h = t >> 4, chunk = t & 15;
-    const size_t src = (size_t)i * (kKvRowElems * 2 / 16) + h * (kHeadBytes / 16) + chunk;
-    // (block, head h, slot) tile offset: head stride is 16 slots of 256 bytes
-    const size_t d = (size_t)dst + (size_t)h * kBlockSize * (kHeadBytes / 16) + chunk;
-    if (threadIdx.x < 128) {
-        k_cache[d] = k_new[src];
-    } else {
-        v_cache[d] = v_new[src];
+    constexpr int kRowChunks = kKvRowElems * 2 / 16;   // 128 chunks of 16 bytes per row and tensor
+    const size_t src = (size_t)i * kRowChunks;
+#pragma unroll
+    for (int k = 0; k < kRowChunks / 32; ++k) {
+        const int j = k * 32 + lane;
+        const int h = j >> 4, chunk = j & 15;
+        // (block, head h, slot) tile offset: head stride is 16 slots of 256 bytes
+        const size_t d = (size_t)dst + (size_t)h * kBlockSize * (kHeadBytes / 16) + chunk;
+        const uint4 kv = k_new[src + j];
+        const uint4 vv = v_new[src + j];
+        k_cache[d] = kv;
+        v_cache[d] = vv;
     }
 }
 
@@ -81,9 +99,10 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t
                              void* v_cache, const int32_t* refcnt, int num_blocks, uint32_t* err,
                              cudaStream_t stream) {
     if (num_tokens <= 0) return cudaSuccess;
-    kv_append_kernel<<<num_tokens, 256, 0, stream>>>(
+    const int grid = (num_tokens + kAppendRowsPerCta - 1) / kAppendRowsPerCta;
+    kv_append_kernel<<<grid, 256, 0, stream>>>(
         static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), cu, ctx, tables, max_blocks, num_reqs,
-        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), refcnt, num_blocks, err);
+        num_tokens, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), refcnt, num_blocks, err);
     return cudaGetLastError();
 }
 
