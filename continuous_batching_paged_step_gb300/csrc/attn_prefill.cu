@@ -317,53 +317,69 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tmap_q, const CUt
             // ------------------------------------------------------------ MMA issuer
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, 1);
+            // Descriptors are built once: Q tiles, K stages and V stages are 32 KiB apart
+            // and a K step moves 32 bytes inside the swizzle rows (or to the next 64-dim
+            // half), so every MMA's operands are a constant step from these bases (the
+            // 14-bit address field never carries: shared addresses stay below 227 KiB).
+            // With a descriptor rebuilt per MMA, this one thread, not the tensor core,
+            // set the pace.
+            constexpr uint64_t kStep32K = (2 * kHalfBytes) >> 4;
+            const uint64_t q_desc0 = smem_desc_sw128(smem_u32(S.q[0][0]), 16, 1024);
+            const uint64_t k_desc0 = smem_desc_sw128(smem_u32(S.k[0][0]), 16, 1024);
+            const uint64_t v_desc0 = smem_desc_sw128(smem_u32(S.v[0][0]), kHalfBytes, 1024);
             bool ok = mbar_wait(&S.q_full, 0);
-            auto issue_qk = [&](int t, int kt) -> bool {
+            // Waits and issues are kept apart: each round first waits for everything it
+            // needs (the next K tile, which is normally long there, then this tile's P and
+            // V), then issues P.V and the next Q K^T back to back, so that the tensor core
+            // has 16 MMAs queued while the thread waits for the other tile.
+            auto wait_k = [&](int kt) -> bool {
+                return mbar_wait(&S.k_full[kt % kKStages], (kt / kKStages) & 1);
+            };
+            auto wait_pv = [&](int t, int kt) -> bool {
+                return mbar_wait(&S.p_full[t], kt & 1) && mbar_wait(&S.v_full[kt % kVStages], (kt / kVStages) & 1);
+            };
+            auto mma_qk = [&](int t, int kt) {
                 const int s = kt % kKStages;
-                if (!mbar_wait(&S.k_full[s], (kt / kKStages) & 1)) return false;
-                tc_fence_after();
-                const uint32_t sq = smem_u32(S.q[t][0]), sk = smem_u32(S.k[s][0]);
+                const uint64_t qa = q_desc0 + (uint64_t)t * kStep32K, kb = k_desc0 + (uint64_t)s * kStep32K;
+                const uint32_t d = tmem + t * 128;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t koff = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    tc_mma_f16(tmem + t * 128, smem_desc_sw128(sq + koff, 16, 1024),
-                               smem_desc_sw128(sk + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                    const uint64_t koff = (uint64_t)((((kk >> 2) * kHalfBytes) + (kk & 3) * 32) >> 4);
+                    tc_mma_f16(d, qa + koff, kb + koff, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&S.s_full[t]);
                 if (t == 1 || kt >= nB) tc_commit(&S.k_empty[s]);   // last QK that reads this K stage
-                return true;
             };
-            auto issue_pv = [&](int t, int kt) -> bool {
+            auto mma_pv = [&](int t, int kt) {
                 const int s = kt % kVStages;
-                if (!mbar_wait(&S.p_full[t], kt & 1) || !mbar_wait(&S.v_full[s], (kt / kVStages) & 1)) return false;
-                tc_fence_after();
-                const uint32_t sv = smem_u32(S.v[s][0]);
+                const uint64_t vb = v_desc0 + (uint64_t)s * kStep32K;
+                const uint32_t d = tmem + 256 + t * 128, pa = tmem + t * 128;
+                const uint32_t acc0 = kt > 0 ? 1u : 0u;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_f16_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                                  smem_desc_sw128(sv + kk * 2048, kHalfBytes, 1024), idesc_pv,
-                                  (kt > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_f16_ts(d, pa + kk * 8, vb + (uint64_t)((kk * 2048) >> 4), idesc_pv, kk > 0 ? 1u : acc0);
                 if (t == 1 || kt >= nB) tc_commit(&S.v_empty[s]);   // last P V that reads this V stage
-                return true;
             };
-            if (ok && nA > 0) ok = issue_qk(0, 0);
-            if (ok && nB > 0) ok = issue_qk(1, 0);
+            if (ok && n_kt > 0 && (ok = wait_k(0))) {
+                tc_fence_after();
+                if (nA > 0) mma_qk(0, 0);
+                if (nB > 0) mma_qk(1, 0);
+            }
             for (int kt = 0; kt < n_kt && ok; ++kt) {
+                const bool more = kt + 1 < n_kt;   // the next K tile is needed by some MMA tile
                 if (kt < nA) {
-                    if (!(ok = issue_pv(0, kt))) break;
-                    if (kt + 1 < nA) {
-                        if (!(ok = issue_qk(0, kt + 1))) break;
-                    } else {
-                        tc_commit(&S.o_done[0]);
-                    }
+                    if (!(ok = (!more || wait_k(kt + 1)) && wait_pv(0, kt))) break;
+                    tc_fence_after();
+                    mma_pv(0, kt);
+                    if (kt + 1 < nA) mma_qk(0, kt + 1);
+                    else tc_commit(&S.o_done[0]);
                 }
                 if (kt < nB) {
-                    if (!(ok = issue_pv(1, kt))) break;
-                    if (kt + 1 < nB) {
-                        if (!(ok = issue_qk(1, kt + 1))) break;
-                    } else {
-                        tc_commit(&S.o_done[1]);
-                    }
+                    if (!(ok = (!more || wait_k(kt + 1)) && wait_pv(1, kt))) break;
+                    tc_fence_after();
+                    mma_pv(1, kt);
+                    if (kt + 1 < nB) mma_qk(1, kt + 1);
+                    else tc_commit(&S.o_done[1]);
                 }
             }
             if (!ok) raise_error(a.err, kErrTimeout);
