@@ -251,66 +251,73 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tmap_q, const CUt
     tc_fence_after();
     const uint32_t tmem = S.tmem_base;
 
-    if ((warp == 0 || warp == 2) && lane == 0) {
+    if (warp == 0 || warp == 2) {
         // ---------------------------------------------- TMA producers: K (warp 0), V (warp 2)
+        // A key tile is 8 blocks x 2 halves of 64 dims = 16 TMA loads; lane j of the warp
+        // issues load j (block j / 2, half j % 2), so a tile's loads leave in one go
+        // instead of one after another from a single thread.
         const bool is_k = warp == 0;
         const CUtensorMap* tm = is_k ? &tmap_k : &tmap_v;
         const int nst = is_k ? kKStages : kVStages;
-        prefetch_tmap(tm);
+        constexpr int kPages = kKeyTile / kBlockSize;
+        const int jb = lane >> 1, jh = lane & 1;          // this lane's block and half (lanes < 16)
+        if (lane == 0) prefetch_tmap(tm);
         if (is_k) {
-            prefetch_tmap(&tmap_q);
-            mbar_arrive_expect_tx(&S.q_full, 4 * kHalfBytes);
-            for (int t = 0; t < 2; ++t) {
-                tma_load_3d(S.q[t][0], &tmap_q, 0, g * kGroup, row0 + kMmaTokens * t, &S.q_full);
-                tma_load_3d(S.q[t][1], &tmap_q, 64, g * kGroup, row0 + kMmaTokens * t, &S.q_full);
+            if (lane == 0) {
+                prefetch_tmap(&tmap_q);
+                mbar_arrive_expect_tx(&S.q_full, 4 * kHalfBytes);
+            }
+            __syncwarp();
+            if (lane < 4) {
+                const int t = lane >> 1, h = lane & 1;
+                tma_load_3d(S.q[t][h], &tmap_q, h * 64, g * kGroup, row0 + kMmaTokens * t, &S.q_full);
             }
         }
         const int32_t* trow = a.tables + (size_t)r * a.max_blocks;
-        constexpr int kPages = kKeyTile / kBlockSize;
-        // block-table entries of key tile kt, read one tile ahead so their latency
-        // overlaps the wait for a free stage
-        int next[kPages];
-        auto read_rows = [&](int kt, int (&dst)[kPages]) {
-            const int pg0 = kt * kPages;
-#pragma unroll
-            for (int j = 0; j < kPages; ++j) dst[j] = (kt < n_kt && pg0 + j < n_pages) ? trow[pg0 + j] : 0;
+        // block-table entry of this lane's block in key tile kt (lanes 0..7 load, the
+        // others take it by shuffle), read one tile ahead so its latency overlaps the wait
+        // for a free stage
+        auto read_entry = [&](int kt) -> int {
+            const int pg = kt * kPages + lane;
+            const int e = (lane < kPages && kt < n_kt && pg < n_pages) ? trow[pg] : 0;
+            return __shfl_sync(0xffffffffu, e, jb & (kPages - 1));
         };
-        read_rows(0, next);
+        int next = read_entry(0);
         int issued = 0;
+        bool ok = true;
         for (int kt = 0; kt < n_kt; ++kt) {
             const int s = kt % nst;
             const uint32_t ph = (kt / nst) & 1;
-            int rows[kPages];
-#pragma unroll
-            for (int j = 0; j < kPages; ++j) {
-                int b = next[j];
-                if ((unsigned)b >= (unsigned)a.num_blocks) {
-                    if (is_k) raise_error(a.err, kErrBadBlock);
-                    b = 0;
-                }
-                rows[j] = (b * kNumKvHeads + g) * kBlockSize;
+            int b = next;
+            if ((unsigned)b >= (unsigned)a.num_blocks) {
+                if (is_k && jh == 0) raise_error(a.err, kErrBadBlock);
+                b = 0;
             }
-            read_rows(kt + 1, next);
+            const int row = (b * kNumKvHeads + g) * kBlockSize;
+            next = read_entry(kt + 1);
             uint64_t* empty = is_k ? &S.k_empty[s] : &S.v_empty[s];
             uint64_t* full = is_k ? &S.k_full[s] : &S.v_full[s];
-            uint8_t* dst = is_k ? S.k[s][0] : S.v[s][0];
-            if (!mbar_wait(empty, ph ^ 1)) {
-                raise_error(a.err, kErrTimeout);
+            ok = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(empty, ph ^ 1) : 0, 0) != 0;
+            if (!ok) {
+                if (lane == 0) raise_error(a.err, kErrTimeout);
                 break;
             }
             const int npg = min(kPages, n_pages - kt * kPages);
-            mbar_arrive_expect_tx(full, npg * kTileBytes);
-            for (int j = 0; j < npg; ++j) {
-                tma_load_2d(dst + j * 2048, tm, 0, rows[j], full);
-                tma_load_2d(dst + kHalfBytes + j * 2048, tm, 64, rows[j], full);
+            if (lane == 0) mbar_arrive_expect_tx(full, npg * kTileBytes);
+            __syncwarp();
+            if (jb < npg && lane < 2 * kPages) {
+                const uint32_t d0 = smem_u32(is_k ? S.k[s][0] : S.v[s][0]);
+                tma_load_2d_u32(d0 + jh * kHalfBytes + jb * 2048, tm, jh * 64, row, smem_u32(full));
             }
             ++issued;
         }
         // Drain: wait until every copy issued into this CTA's shared memory landed.
-        if (is_k && !mbar_wait(&S.q_full, 0)) raise_error(a.err, kErrTimeout);
-        for (int kt = issued - nst < 0 ? 0 : issued - nst; kt < issued; ++kt) {
-            uint64_t* full = is_k ? &S.k_full[kt % nst] : &S.v_full[kt % nst];
-            if (!mbar_wait(full, (kt / nst) & 1)) raise_error(a.err, kErrTimeout);
+        if (lane == 0) {
+            if (is_k && !mbar_wait(&S.q_full, 0)) raise_error(a.err, kErrTimeout);
+            for (int kt = issued - nst < 0 ? 0 : issued - nst; kt < issued; ++kt) {
+                uint64_t* full = is_k ? &S.k_full[kt % nst] : &S.v_full[kt % nst];
+                if (!mbar_wait(full, (kt / nst) & 1)) raise_error(a.err, kErrTimeout);
+            }
         }
     } else if (warp == 1) {
         if (lane == 0) {
