@@ -185,3 +185,26 @@ def test_full_size_configs_sampled(runner, name):
             assert np.array_equal(v[b, :, off, :].reshape(-1), inp.v_new[i])
     finally:
         step.close()
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_random_step_shapes(runner, case):
+    # Random packed steps: empty requests, decode rows and prefill chunks in any order,
+    # contexts from 0 to ~2,000 (log-uniform, so short and block-boundary ones are common),
+    # a random decode CTA cap; the whole output and the pool are checked.
+    rng = np.random.default_rng(9000 + case)
+    R = int(rng.integers(1, 24))
+    q_lens, ctx_lens = [], []
+    for _ in range(R):
+        kind = rng.random()
+        q = 0 if kind < 0.08 else 1 if kind < 0.65 else int(rng.integers(2, 160))
+        c = int(np.exp(rng.uniform(0, np.log(2100)))) - 1 if rng.random() < 0.9 else int(rng.integers(0, 3)) * 16
+        q_lens.append(q)
+        ctx_lens.append(c)
+    need = sum(-(-(c + q) // 16) for c, q in zip(ctx_lens, q_lens))
+    spec = wl.StepSpec(f"random-{case}", q_lens=q_lens, ctx_lens=ctx_lens, num_blocks=need + int(rng.integers(1, 64)),
+                       seed=7000 + case)
+    if spec.num_tokens == 0:
+        spec.q_lens[0] = 1
+    ctas = [0, 1, 3, 16][case % 4]
+    _run_full_check(runner, spec, ctas=ctas)
