@@ -1,4 +1,4 @@
-// Decode rows (q_len == 1): split-KV paged attention on CUDA cores, HBM-bound.
+// Decode rows (q_len == 1): split-KV paged attention, HBM-bound.
 //
 // The decode formula of page "Continuous Batching" (k4i.top), section "与 KV cache 的关
 // 系": the row's query attends to [K_cache; k_t] and [V_cache; v_t] of its own request,
@@ -11,31 +11,39 @@
 //   ranges, one per CTA (one CTA per SM of the decode's share of the SMs, which the step's
 //   metadata kernel sizes so that the prefill tiles run on the others; fewer CTAs when
 //   there are under 4 blocks per CTA; more, in whole waves, when a range would exceed the
-//   2,048 block ids a CTA stages).  A
-//   CTA walks its range request by request; a request cut by a range boundary produces one
-//   partial per CTA that touches it (slot r + cta), merged by whichever of those CTAs
-//   finishes last; a request inside one range is finished in place.
+//   2,048 block ids a CTA stages).  A CTA walks its range request by request; a request
+//   cut by a range boundary produces one partial per CTA that touches it (slot r + cta),
+//   merged by whichever of those CTAs finishes last; a request inside one range is
+//   finished in place.
 // * The CTA first looks up the physical ids of all its blocks in parallel (into shared
 //   memory), so no table lookup sits between a freed buffer and its refill.
-// * One block of all 8 KV heads is 32 KiB contiguous in the pool, so each block of K and
-//   of V arrives with ONE bulk copy (cp.async.bulk, mbarrier completion) into a 3-stage
-//   ring of 64 KiB stages; the last of the 16 warps to finish with a stage refills it
-//   with the block three ahead (no thread waits for the others to do so).
-// * GQA packing: the 4 query heads of a KV head share every K/V byte read.  Two warps
-//   per KV head (16 warps) split each block's 16 tokens 8/8, with separate
-//   online-softmax states merged at the end of a request segment.
-// * Scores: a lane holds 16 of the 128 dims (8 lanes per token) of 2 tokens for all 4
-//   query heads; packed fp32x2 FMAs; a transpose-reduce over the 8 lanes (7 shuffles)
-//   leaves one finished (token, head) score per lane.  Online softmax in base 2 (the
-//   query is pre-scaled by softmax_scale * log2 e) against a reference max per head that
-//   moves only when a score exceeds it by more than 2^8 (a warp vote; the max reduction
-//   and the rescale run only then), with per-lane partial sums reduced once per segment.
-// * P.V: a lane owns 4 output dims of all 4 heads; weights of the warp's 8 tokens go
-//   through a per-warp shared-memory slot as duplicated pairs for the packed FMAs.
+// * One block of all 8 KV heads is 128 rows (head x token) of 128 dims in the pool, so
+//   its K and its V arrive with four tensor-map loads (one per 64-dim half, 128-byte
+//   swizzle) into a 3-stage ring of 64 KiB stages; the last of the 8 warps to finish
+//   with a stage refills it with the block three ahead (no thread waits for the others
+//   to do so).
+// * One warp per KV head.  Its 4 query heads share every K/V byte (GQA packing), and the
+//   two contractions of a block are small matrix products, which run on the tensor
+//   cores (mma.sync m16n8k16, bf16 operands, fp32 accumulation) instead of as thousands
+//   of scalar FMAs:  S^T = K Q^T (16 tokens x 8 columns, the 4 query heads and 4 zero
+//   columns) and O^T += V^T P^T (128 dims x 8 columns).  K and V fragments come from
+//   the swizzled tiles with ldmatrix (V transposed on the way), so reads are free of
+//   bank conflicts; the weights go from the score fragment to the P^T operand with one
+//   register transpose (movmatrix) per 8 tokens.
+// * Online softmax in base 2 (scores x softmax_scale x log2 e) against a reference max
+//   per head that moves only when a score exceeds it by more than 2^8 (a warp vote; the
+//   max reduction and the rescale run only then), with per-lane partial sums reduced
+//   once per request segment.  Weights enter P.V rounded to bf16; the sums use them
+//   unrounded.
 // Partial results keep (m, l, unnormalised acc); the last CTA to finish a split row
 // (an arrival count per row) merges them: O = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M)
 // l_s with M = max_s m_s.
-// Keys at positions >= ctx + 1 of the last block are excluded (score -inf, value unread).
+// A warp reads all of its K and V fragments of a block into registers before anything
+// else and releases the stage at once, so a stage is held only for those reads.
+// Keys at positions >= ctx + 1 of the last block are excluded: score -inf, and their V
+// values zeroed in the fragments (stale bytes could hold NaN, and 0 x NaN is NaN).
+#include <cuda.h>
+
 #include "kvp_device.cuh"
 #include "kvp_launch.h"
 
@@ -43,32 +51,80 @@ namespace kvp {
 
 namespace {
 
-constexpr int kDecWarps = 16;
+constexpr int kDecWarps = kNumKvHeads;   // one warp per KV head
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDecStages = 3;
-constexpr int kTokensPerWarp = kBlockSize / 2;
+constexpr int kBlockRows = kNumKvHeads * kBlockSize;   // rows (head, token) of one block: 128
+constexpr int kHalfTile = kBlockRows * 128;            // one block's 64-dim half: 128 rows x 128 B
+constexpr int kStageBytes = 4 * kHalfTile;             // K and V, two halves each: 64 KiB
 
 constexpr int kIdCap = 2048;   // block ids a CTA stages in shared memory (its whole range)
 
-struct __align__(128) DecodeSmem {
-    uint8_t kv[kDecStages][2][kBlockBytes];           // [stage][K|V][8 heads x 16 x 128 bf16]
-    int32_t ids[kIdCap];                              // physical block of each block of the range
-    float2 pbuf[kDecWarps][kTokensPerWarp][kGroup];   // (p, p) per token and head
-    float2 abuf[kDecWarps][kGroup];                   // (alpha, alpha) per head
-    float2 merge_acc[kNumKvHeads][32][8];             // second half's accumulators
-    float merge_ml[kNumKvHeads][8];                   // second half's m[4], l[4]
-    int pair_abort[kNumKvHeads];
+struct __align__(1024) DecodeSmem {
+    uint8_t kv[kDecStages][2][2][kHalfTile];   // [stage][K|V][dim half][row 16 h + token], 128-byte swizzle
+    int32_t ids[kIdCap];                       // physical block of each block of the range
     int cta_abort;
     int merge_last;
     int first_req, last_req;
-    unsigned released[kDecStages];                    // warps done with a stage (mod 16)
-    int issued;                                       // blocks issued so far
-    int n_rel;                                        // blocks in the range
-    const uint8_t* cache[2];                          // K and V pools
-    uint32_t* err;
+    unsigned released[kDecStages];             // warps done with a stage (mod 8)
+    int issued;                                // blocks issued so far
+    int n_rel;                                 // blocks in the range
     uint64_t policy;
     uint64_t full[kDecStages];
 };
+
+// Tensor-map load with an L2 eviction hint.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* tmap, int c0, int c1, uint32_t bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Four 8x8 bf16 matrices from shared memory (lanes 8j..8j+7 give the row addresses of
+// matrix j); .trans delivers each matrix transposed.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// d += A (16x16, row-major fragments) x B (16x8, column fragments), bf16 in, fp32 out.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 bf16 matrix held one row pair per lane (lane 4i + j holds row i,
+// columns 2j and 2j + 1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// Copy K and V of block `q` of the range into stage `st`.
+__device__ __forceinline__ void issue_block(DecodeSmem& S, const CUtensorMap* tk, const CUtensorMap* tv, int st,
+                                            int q) {
+    const int y = S.ids[q] * kBlockRows;
+    const uint32_t bar = smem_u32(&S.full[st]);
+    const uint32_t d = smem_u32(S.kv[st][0][0]);
+    mbar_arrive_expect_tx(&S.full[st], kStageBytes);
+    tma_load_2d_hint(d, tk, 0, y, bar, S.policy);
+    tma_load_2d_hint(d + kHalfTile, tk, 64, y, bar, S.policy);
+    tma_load_2d_hint(d + 2 * kHalfTile, tv, 0, y, bar, S.policy);
+    tma_load_2d_hint(d + 3 * kHalfTile, tv, 64, y, bar, S.policy);
+    atomicMax(&S.issued, q + 1);
+}
 
 // atom.add with acquire-release ordering at CTA scope (shared memory).
 __device__ __forceinline__ unsigned atomic_add_acq_rel_cta(unsigned* p, unsigned v) {
@@ -77,47 +133,19 @@ __device__ __forceinline__ unsigned atomic_add_acq_rel_cta(unsigned* p, unsigned
     return old;
 }
 
-__device__ __forceinline__ void named_bar(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
-
-// Partial dot products of one token's 16-dim slice (chunks dg and dg + 8 of its 256-byte
-// K row) with the 4 query heads' matching slices.
-__device__ __forceinline__ void token_scores(const float2 (&q2)[kGroup][8], const uint8_t* krow, int dg,
-                                             float (&v)[kGroup]) {
-    const uint4 ka = *reinterpret_cast<const uint4*>(krow + dg * 16);
-    const uint4 kb = *reinterpret_cast<const uint4*>(krow + 128 + dg * 16);
-    const uint32_t w[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-    float2 s[kGroup];
-#pragma unroll
-    for (int g = 0; g < kGroup; ++g) s[g] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float2 k = bf16x2_to_f2(w[i]);
-#pragma unroll
-        for (int g = 0; g < kGroup; ++g) s[g] = __ffma2_rn(q2[g][i], k, s[g]);
-    }
-#pragma unroll
-    for (int g = 0; g < kGroup; ++g) v[g] = s[g].x + s[g].y;
-}
-
-// acc[g] += p[g] * v for one token: v is the lane's 4 dims of the token's V row, p the
-// token's weight for each of the 4 query heads (stored as duplicated pairs).
-__device__ __forceinline__ void pv_token(const float2 (&pt)[kGroup], const uint8_t* vrow, int lane,
-                                         float2 (&acc)[kGroup][2]) {
-    const uint2 vv = *reinterpret_cast<const uint2*>(vrow + lane * 8);
-    const float2 va = bf16x2_to_f2(vv.x), vb = bf16x2_to_f2(vv.y);
-    const float4 p01 = *reinterpret_cast<const float4*>(&pt[0]);
-    const float4 p23 = *reinterpret_cast<const float4*>(&pt[2]);
-    const float2 pg[4] = {make_float2(p01.x, p01.y), make_float2(p01.z, p01.w), make_float2(p23.x, p23.y),
-                          make_float2(p23.z, p23.w)};
-#pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
-        acc[g][0] = __ffma2_rn(va, pg[g], acc[g][0]);
-        acc[g][1] = __ffma2_rn(vb, pg[g], acc[g][1]);
-    }
+// Lane 0 of a warp that is done reading block `rel` (stage st; the warp's reads are
+// ordered before this by __syncwarp): the last of the 8 warps refills the stage with
+// block rel + kDecStages.  One shared atomic per warp and block: the count both elects
+// the refilling warp and orders every warp's accesses (release) before the copy
+// (acquire, then a proxy fence for the tensor copy's write).
+__device__ __forceinline__ void release_stage(DecodeSmem& S, const CUtensorMap* tk, const CUtensorMap* tv, int st,
+                                              int rel) {
+    const unsigned old = atomic_add_acq_rel_cta(&S.released[st], 1u);
+    if ((old & (kDecWarps - 1)) != kDecWarps - 1) return;
+    const int q = rel + kDecStages;
+    if (q >= S.n_rel) return;
+    fence_proxy_async_smem();
+    issue_block(S, tk, tv, st, q);
 }
 
 // A decode CTA streams at least this many blocks: with fewer blocks than CTAs x this,
@@ -145,68 +173,65 @@ __device__ __forceinline__ int owner_cta(int x, int P, int G) {
 }
 
 
-// Copy K and V of block `q` of the range into stage `st`.
-__device__ __noinline__ void issue_block(DecodeSmem& S, int st, int q) {
-    const size_t off = (size_t)S.ids[q] * kBlockBytes;
-    mbar_arrive_expect_tx(&S.full[st], 2 * kBlockBytes);
-    bulk_load(S.kv[st][0], S.cache[0] + off, kBlockBytes, &S.full[st], S.policy);
-    bulk_load(S.kv[st][1], S.cache[1] + off, kBlockBytes, &S.full[st], S.policy);
-    atomicMax(&S.issued, q + 1);
-}
-
-// Lane 0 of a warp that is done reading block `rel` (stage st; the warp's reads are
-// ordered before this by __syncwarp): the last of the 16 warps refills the stage with
-// block rel + kDecStages.  One shared atomic per warp and block: the count both elects
-// the refilling warp and orders every warp's reads (release) before the copy (acquire,
-// then a proxy fence for the bulk copy's write).
-__device__ __forceinline__ void release_stage(DecodeSmem& S, int st, int rel) {
-    const unsigned old = atomic_add_acq_rel_cta(&S.released[st], 1u);
-    if ((old & (kDecWarps - 1)) != kDecWarps - 1) return;
-    const int q = rel + kDecStages;
-    if (q >= S.n_rel) return;
-    fence_proxy_async_smem();
-    issue_block(S, st, q);
-}
-
 // Merge the partial results of a decode row whose blocks were split over CTAs c0..c1
-// (all 512 threads of the CTA: thread t takes query head t / 16 and dims 8 (t % 16) ..
-// 8 (t % 16) + 7).  O = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c.
+// (all 256 threads of the CTA: thread t takes query head t / 8 and dims 16 (t % 8) ..
+// 16 (t % 8) + 15).  O = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c.
 __device__ __noinline__ void merge_partials(int r, int row, int c0, int c1, const float* part_acc,
                                             const float2* part_ml, __nv_bfloat16* out) {
-    const int head = threadIdx.x >> 4, d0 = (threadIdx.x & 15) * 8;
+    const int head = threadIdx.x >> 3, d0 = (threadIdx.x & 7) * 16;
     float M = -INFINITY;
     for (int c = c0; c <= c1; ++c) M = fmaxf(M, __ldcg(&part_ml[((size_t)r + c) * kNumQHeads + head]).x);
     const float Mu = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f, o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float L = 0.f, o[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i] = 0.f;
     for (int c = c0; c <= c1; ++c) {
         const size_t sh = ((size_t)r + c) * kNumQHeads + head;
         const float2 ml = __ldcg(&part_ml[sh]);
         const float w = fast_exp2(ml.x - Mu);
         L = fmaf(ml.y, w, L);
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(part_acc + sh * kHeadDim + d0));
-        const float4 b = __ldcg(reinterpret_cast<const float4*>(part_acc + sh * kHeadDim + d0 + 4));
-        o[0] = fmaf(a.x, w, o[0]); o[1] = fmaf(a.y, w, o[1]); o[2] = fmaf(a.z, w, o[2]); o[3] = fmaf(a.w, w, o[3]);
-        o[4] = fmaf(b.x, w, o[4]); o[5] = fmaf(b.y, w, o[5]); o[6] = fmaf(b.z, w, o[6]); o[7] = fmaf(b.w, w, o[7]);
+        const float4* src = reinterpret_cast<const float4*>(part_acc + sh * kHeadDim + d0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 a = __ldcg(src + j);
+            o[4 * j + 0] = fmaf(a.x, w, o[4 * j + 0]);
+            o[4 * j + 1] = fmaf(a.y, w, o[4 * j + 1]);
+            o[4 * j + 2] = fmaf(a.z, w, o[4 * j + 2]);
+            o[4 * j + 3] = fmaf(a.w, w, o[4 * j + 3]);
+        }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    uint4 wv;
-    wv.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-    wv.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-    wv.z = pack_bf16x2(o[4] * inv, o[5] * inv);
-    wv.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-    *reinterpret_cast<uint4*>(out + (size_t)row * kQRowElems + head * kHeadDim + d0) = wv;
+    uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * kQRowElems + head * kHeadDim + d0);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        uint4 wv;
+        wv.x = pack_bf16x2(o[8 * j + 0] * inv, o[8 * j + 1] * inv);
+        wv.y = pack_bf16x2(o[8 * j + 2] * inv, o[8 * j + 3] * inv);
+        wv.z = pack_bf16x2(o[8 * j + 4] * inv, o[8 * j + 5] * inv);
+        wv.w = pack_bf16x2(o[8 * j + 6] * inv, o[8 * j + 7] * inv);
+        dst[j] = wv;
+    }
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
+    const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
     const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out, const int32_t* __restrict__ cu,
     const int32_t* __restrict__ ctx, const int32_t* __restrict__ tables, int max_blocks, int num_blocks,
-    const uint8_t* __restrict__ k_cache, const uint8_t* __restrict__ v_cache, const int32_t* __restrict__ page_off,
-    int num_reqs, int wave, const int32_t* __restrict__ counters, float* __restrict__ part_acc,
-    float2* __restrict__ part_ml,
-    int32_t* __restrict__ seg_count, float scale_log2, uint32_t* __restrict__ err) {
+    const int32_t* __restrict__ page_off, int num_reqs, int wave, const int32_t* __restrict__ counters,
+    float* __restrict__ part_acc, float2* __restrict__ part_ml, int32_t* __restrict__ seg_count, float scale_log2,
+    uint32_t* __restrict__ err) {
     extern __shared__ uint8_t smem_raw[];
-    DecodeSmem& S = *reinterpret_cast<DecodeSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    DecodeSmem& S =
+        *reinterpret_cast<DecodeSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+    }
     grid_dep_wait();     // block offsets, cache contents
     grid_dep_launch();
     const int P = page_off[num_reqs];
@@ -238,14 +263,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
         }
         S.issued = 0;
         S.n_rel = n_rel;
-        S.cache[0] = k_cache;
-        S.cache[1] = v_cache;
-        S.err = err;
         S.policy = policy_evict_first();
         S.cta_abort = 0;
         fence_barrier_init();
     }
-    if (threadIdx.x < kNumKvHeads) S.pair_abort[threadIdx.x] = 0;
     // requests holding the first and the last block of the range (one parallel pass)
     for (int r = threadIdx.x; r < num_reqs; r += kDecThreads) {
         const int a0 = page_off[r], a1 = page_off[r + 1];
@@ -273,14 +294,31 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int j = 0; j < kDecStages && j < n_rel; ++j) issue_block(S, j, j);
+        for (int j = 0; j < kDecStages && j < n_rel; ++j) issue_block(S, &tmap_k, &tmap_v, j, j);
+
     }
 
-    const int h = warp >> 1, half = warp & 1;
-    const int dg = lane & 7;                      // dims 8dg..8dg+7 and 64+8dg..64+8dg+7
-    const int tl = lane >> 3;                     // token within a group of 4
-    const int my_tok = (lane & 1) * 4 + tl;       // token (of the warp's 8) whose score this lane ends with
-    const int hd = ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);  // ... and its head
+    // Fragment coordinates (PTX mma.m16n8k16 layouts): lane = 4 g + t.  A fragment rows
+    // are tokens (S^T) or dims (O^T); B columns and C columns are the query heads, of
+    // which columns 0..3 are real (lanes with t < 2 hold them in C).
+    const int h = warp;
+    const int g = lane >> 2, t = lane & 3;
+    const int x7 = lane & 7;
+    // ldmatrix row addresses inside a stage's K (V) region, 64-dim half 0: K row = token
+    // x7 + 8 (lane bit 3), 16-byte chunk 2j + (lane bit 4) of the k-step's 32 bytes; V row
+    // = token x7 + 8 (lane bit 4), chunk 2j + (lane bit 3); 128-byte swizzle: chunk ^ row % 8.
+    uint32_t k_off[4], v_off[4];
+    {
+        const uint32_t k_row = (uint32_t)(h * kBlockSize + x7 + 8 * ((lane >> 3) & 1)) * 128;
+        const uint32_t v_row = (uint32_t)(h * kBlockSize + x7 + 8 * (lane >> 4)) * 128;
+        const uint32_t k_cb = lane >> 4, v_cb = (lane >> 3) & 1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            k_off[j] = k_row + ((((uint32_t)(2 * j) + k_cb) ^ (uint32_t)x7) << 4);
+            v_off[j] = v_row + ((((uint32_t)(2 * j) + v_cb) ^ (uint32_t)x7) << 4);
+        }
+    }
+    const uint32_t ring0 = smem_u32(S.kv[0][0][0]);
     int stage = 0;
     uint32_t phase = 0;
     bool aborted = false;
@@ -294,99 +332,111 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
         const int row = cu[r];
         const int n_keys = ctx[r] + 1;
 
-        float2 q2[kGroup][8];
+        // Q^T as the B operand of S^T = K Q^T: k-step s covers dims 16 s .. 16 s + 15; lane
+        // (g, t) holds head g's dims 16 s + 2 t, +1 and 16 s + 2 t + 8, +9 (zero for g >= 4)
+        uint32_t qb[8][2];
+        {
+            const uint32_t* qw = reinterpret_cast<const uint32_t*>(q + (size_t)row * kQRowElems +
+                                                                    (h * kGroup + (g & 3)) * kHeadDim);
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g) {
-            const uint4* qp = reinterpret_cast<const uint4*>(q + (size_t)row * kQRowElems + (h * kGroup + g) * kHeadDim);
-            const uint4 a = qp[dg], b = qp[8 + dg];
-            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float2 f = bf16x2_to_f2(w[i]);
-                q2[g][i] = make_float2(f.x * scale_log2, f.y * scale_log2);
+            for (int s = 0; s < 8; ++s) {
+                qb[s][0] = g < kGroup ? __ldg(qw + 8 * s + t) : 0u;
+                qb[s][1] = g < kGroup ? __ldg(qw + 8 * s + 4 + t) : 0u;
             }
         }
-        float m_ref = -INFINITY, l_part = 0.f;   // per head hd (m_ref uniform over its lanes)
-        float2 acc[kGroup][2];
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // heads 2t, 2t + 1
+        float o[8][4];
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g) acc[g][0] = acc[g][1] = make_float2(0.f, 0.f);
+        for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
         for (; page < seg_end; ++page) {
-            if (!aborted && !mbar_wait(&S.full[stage], phase)) {
-                raise_error(err, kErrTimeout);
+            if (!aborted && *reinterpret_cast<volatile int*>(&S.cta_abort)) aborted = true;   // another warp gave up
+            if (!aborted && !warp_wait(&S.full[stage], phase)) {
+                if (lane == 0) {
+                    raise_error(err, kErrTimeout);
+                    S.cta_abort = 1;
+                }
                 aborted = true;
             }
             if (!aborted) {
-                const uint8_t* kt = S.kv[stage][0] + h * kTileBytes + half * kTokensPerWarp * kHeadBytes;
-                const int pos0 = (page - req_lo) * kBlockSize + half * kTokensPerWarp;
-                const int n_valid = min(kTokensPerWarp, n_keys - pos0);   // >= 1 except in a last block
-                // ---- scores of tokens tl and 4 + tl, all 4 heads
-                const uint8_t* k0 = kt + tl * kHeadBytes;
-                float v0[kGroup], v1[kGroup];
-                token_scores(q2, k0, dg, v0);
-                token_scores(q2, k0 + 4 * kHeadBytes, dg, v1);
-                // transpose-reduce over the 8 lanes of a token: bit 2 picks the head pair,
-                // bit 1 the head, bit 0 the token
-                const bool b2 = (lane >> 2) & 1, b1 = (lane >> 1) & 1, b0 = lane & 1;
-                float x[4], y[4];
-                x[0] = b2 ? v0[2] : v0[0];
-                x[1] = b2 ? v0[3] : v0[1];
-                x[2] = b2 ? v1[2] : v1[0];
-                x[3] = b2 ? v1[3] : v1[1];
-                y[0] = b2 ? v0[0] : v0[2];
-                y[1] = b2 ? v0[1] : v0[3];
-                y[2] = b2 ? v1[0] : v1[2];
-                y[3] = b2 ? v1[1] : v1[3];
+                const uint32_t kb = ring0 + stage * kStageBytes, vb = kb + 2 * kHalfTile;
+                const int n_valid = n_keys - (page - req_lo) * kBlockSize;   // >= 1; < 16 only in a last block
+                // All of this warp's reads of the stage first (K and V fragments into
+                // registers), then the stage is released, so the refill starts before the
+                // arithmetic rather than after it.
+                uint32_t ka[8][4], va[8][4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) x[k] += __shfl_xor_sync(0xffffffffu, y[k], 4);
-                float u0 = b1 ? x[1] : x[0], u1 = b1 ? x[3] : x[2];
-                const float t0 = b1 ? x[0] : x[1], t1 = b1 ? x[2] : x[3];
-                u0 += __shfl_xor_sync(0xffffffffu, t0, 2);
-                u1 += __shfl_xor_sync(0xffffffffu, t1, 2);
-                float sc = b0 ? u1 : u0;
-                sc += __shfl_xor_sync(0xffffffffu, b0 ? u0 : u1, 1);
-                if (my_tok >= n_valid) sc = -INFINITY;
-                // ---- online softmax for head hd over the warp's 8 tokens.  The reference
-                // max m_ref moves only when a score exceeds it by more than 2^8 (then the
-                // warp reduces the max and rescales); the sum stays a per-lane partial
-                // until the segment ends.  Weights are 2^(s - m_ref) <= 2^8.
-                if (__any_sync(0xffffffffu, sc > m_ref + 8.f)) {
-                    float mx = sc;
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                    const float m_new = fmaxf(m_ref, mx);
-                    const float alpha = fast_exp2(m_ref - (m_new == -INFINITY ? 0.f : m_new));
-                    l_part *= alpha;
-                    m_ref = m_new;
-                    if ((lane & 0x19) == 0) S.abuf[warp][hd] = make_float2(alpha, alpha);
-                    __syncwarp();
-                    const float4 al01 = *reinterpret_cast<const float4*>(&S.abuf[warp][0]);
-                    const float4 al23 = *reinterpret_cast<const float4*>(&S.abuf[warp][2]);
-                    const float2 al[4] = {make_float2(al01.x, al01.y), make_float2(al01.z, al01.w),
-                                          make_float2(al23.x, al23.y), make_float2(al23.z, al23.w)};
+                for (int s = 0; s < 8; ++s) ldsm_x4(kb + (s >> 2) * kHalfTile + k_off[s & 3], ka[s]);
 #pragma unroll
-                    for (int g = 0; g < kGroup; ++g) {
-                        acc[g][0] = __fmul2_rn(acc[g][0], al[g]);
-                        acc[g][1] = __fmul2_rn(acc[g][1], al[g]);
-                    }
-                }
-                const float p = fast_exp2(sc - (m_ref == -INFINITY ? 0.f : m_ref));
-                l_part += p;
-                S.pbuf[warp][my_tok][hd] = make_float2(p, p);
+                for (int i = 0; i < 8; ++i) ldsm_x4_t(vb + (i >> 2) * kHalfTile + v_off[i & 3], va[i]);
                 __syncwarp();
-                {
-                    const uint8_t* vt = S.kv[stage][1] + h * kTileBytes + half * kTokensPerWarp * kHeadBytes;
-                    if (n_valid == kTokensPerWarp) {
+                if (lane == 0) release_stage(S, &tmap_k, &tmap_v, stage, page - lo);
+                if (n_valid < kBlockSize) {
+                    // tokens past the end of the request: zero their V values (stale bytes
+                    // could hold NaN, and 0 x NaN is NaN).  V^T fragment registers 0, 1 hold
+                    // tokens 2t, 2t + 1; registers 2, 3 tokens 2t + 8, 2t + 9.
+                    auto keep = [&](int tk) -> uint32_t {
+                        return (tk < n_valid ? 0x0000FFFFu : 0u) | (tk + 1 < n_valid ? 0xFFFF0000u : 0u);
+                    };
+                    const uint32_t k01 = keep(2 * t), k89 = keep(2 * t + 8);
 #pragma unroll
-                        for (int t = 0; t < kTokensPerWarp; ++t)
-                            pv_token(S.pbuf[warp][t], vt + t * kHeadBytes, lane, acc);
-                    } else {
-                        for (int t = 0; t < n_valid; ++t) pv_token(S.pbuf[warp][t], vt + t * kHeadBytes, lane, acc);
+                    for (int i = 0; i < 8; ++i) {
+                        va[i][0] &= k01;
+                        va[i][1] &= k01;
+                        va[i][2] &= k89;
+                        va[i][3] &= k89;
                     }
-                    __syncwarp();
-                    if (lane == 0) release_stage(S, stage, page - lo);
                 }
+                // ---- S^T = K Q^T: 16 tokens x (4 heads + 4 zero columns)
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int s = 0; s < 8; s += 2) {
+                    mma_16816(sa, ka[s], qb[s][0], qb[s][1]);
+                    mma_16816(sb, ka[s + 1], qb[s + 1][0], qb[s + 1][1]);
+                }
+                // lane holds tokens g, g + 8 of heads 2t, 2t + 1: x[0] (g, 2t), x[1] (g, 2t+1),
+                // x[2] (g+8, 2t), x[3] (g+8, 2t+1)
+                float x[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) x[j] = (sa[j] + sb[j]) * scale_log2;
+                if (t >= 2 || g >= n_valid) x[0] = x[1] = -INFINITY;
+                if (t >= 2 || g + 8 >= n_valid) x[2] = x[3] = -INFINITY;
+                // ---- online softmax against the lazily moved reference max
+                const bool need = fmaxf(x[0], x[2]) > m0 + 8.f || fmaxf(x[1], x[3]) > m1 + 8.f;
+                if (__any_sync(0xffffffffu, need)) {
+                    float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                    }
+                    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+                    const float a0 = fast_exp2(m0 - (n0 == -INFINITY ? 0.f : n0));
+                    const float a1 = fast_exp2(m1 - (n1 == -INFINITY ? 0.f : n1));
+                    l0 *= a0;
+                    l1 *= a1;
+                    m0 = n0;
+                    m1 = n1;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        o[i][0] *= a0;
+                        o[i][1] *= a1;
+                        o[i][2] *= a0;
+                        o[i][3] *= a1;
+                    }
+                }
+                const float u0 = m0 == -INFINITY ? 0.f : m0, u1 = m1 == -INFINITY ? 0.f : m1;
+                const float p0 = fast_exp2(x[0] - u0), p1 = fast_exp2(x[1] - u1);
+                const float p2 = fast_exp2(x[2] - u0), p3 = fast_exp2(x[3] - u1);
+                l0 += p0 + p2;
+                l1 += p1 + p3;
+                // P^T as the B operand: lane (g, t) gets head g's weights of tokens 2t, 2t+1
+                // (first 8 tokens) and 2t + 8, 2t + 9 (last 8)
+                const uint32_t pb0 = movmatrix_t(pack_bf16x2(p0, p1));
+                const uint32_t pb1 = movmatrix_t(pack_bf16x2(p2, p3));
+                // ---- O^T += V^T P^T: m-tile i covers dims 16 i .. 16 i + 15
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mma_16816(o[i], va[i], pb0, pb1);
             }
             if (++stage == kDecStages) {
                 stage = 0;
@@ -394,71 +444,53 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
             }
         }
 
-        // ------------------------------------------------ merge the two token halves
-        l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
-        l_part += __shfl_xor_sync(0xffffffffu, l_part, 8);
-        l_part += __shfl_xor_sync(0xffffffffu, l_part, 16);
-        float m[kGroup], l[kGroup];
+        // ------------------------------------------------ finish the segment
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g) {
-            const int src = ((g >> 1) << 2) | ((g & 1) << 1);
-            m[g] = __shfl_sync(0xffffffffu, m_ref, src);
-            l[g] = __shfl_sync(0xffffffffu, l_part, src);
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         }
-        if (aborted && lane == 0) S.pair_abort[h] = 1;
-        if (half == 1) {
+        if (!aborted) {
+            if (whole) {
+                // O = O^T / l, transposed back so that lane (g, t) holds dims 16 i + 2t, +1
+                // and 16 i + 8 + 2t, +1 of head g
+                const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+                uint32_t* orow = reinterpret_cast<uint32_t*>(out + (size_t)row * kQRowElems +
+                                                             (h * kGroup + (g & 3)) * kHeadDim);
 #pragma unroll
-            for (int g = 0; g < kGroup; ++g) {
-                S.merge_acc[h][lane][2 * g] = acc[g][0];
-                S.merge_acc[h][lane][2 * g + 1] = acc[g][1];
-            }
-            if (lane == 0) {
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t w0 = movmatrix_t(pack_bf16x2(o[i][0] * i0, o[i][1] * i1));
+                    const uint32_t w1 = movmatrix_t(pack_bf16x2(o[i][2] * i0, o[i][3] * i1));
+                    if (g < kGroup) {
+                        orow[8 * i + t] = w0;
+                        orow[8 * i + 4 + t] = w1;
+                    }
+                }
+            } else if (t < 2) {
+                const size_t slot = (size_t)r + blockIdx.x;
+                float* pa = part_acc + (slot * kNumQHeads + h * kGroup + 2 * t) * kHeadDim;
 #pragma unroll
-                for (int g = 0; g < kGroup; ++g) {
-                    S.merge_ml[h][g] = m[g];
-                    S.merge_ml[h][4 + g] = l[g];
+                for (int i = 0; i < 8; ++i) {
+                    pa[16 * i + g] = o[i][0];
+                    pa[kHeadDim + 16 * i + g] = o[i][1];
+                    pa[16 * i + 8 + g] = o[i][2];
+                    pa[kHeadDim + 16 * i + 8 + g] = o[i][3];
+                }
+                if (g == 0) {
+                    part_ml[slot * kNumQHeads + h * kGroup + 2 * t] = make_float2(m0, l0);
+                    part_ml[slot * kNumQHeads + h * kGroup + 2 * t + 1] = make_float2(m1, l1);
                 }
             }
         }
-        named_bar(1 + h, 64);
-        const bool pair_aborted = S.pair_abort[h] != 0;
-        if (half == 0 && !pair_aborted) {
-#pragma unroll
-            for (int g = 0; g < kGroup; ++g) {
-                const float m1 = S.merge_ml[h][g], l1 = S.merge_ml[h][4 + g];
-                const float M = fmaxf(m[g], m1);
-                const float Mu = (M == -INFINITY) ? 0.f : M;
-                const float e0 = fast_exp2(m[g] - Mu), e1 = fast_exp2(m1 - Mu);
-                const float L = l[g] * e0 + l1 * e1;
-                const float2 b0 = S.merge_acc[h][lane][2 * g], b1 = S.merge_acc[h][lane][2 * g + 1];
-                const float o0 = acc[g][0].x * e0 + b0.x * e1, o1 = acc[g][0].y * e0 + b0.y * e1;
-                const float o2 = acc[g][1].x * e0 + b1.x * e1, o3 = acc[g][1].y * e0 + b1.y * e1;
-                const int head = h * kGroup + g;
-                if (whole) {
-                    const float inv = L > 0.f ? 1.f / L : 0.f;
-                    uint2 wv;
-                    wv.x = pack_bf16x2(o0 * inv, o1 * inv);
-                    wv.y = pack_bf16x2(o2 * inv, o3 * inv);
-                    *reinterpret_cast<uint2*>(out + (size_t)row * kQRowElems + head * kHeadDim + lane * 4) = wv;
-                } else {
-                    const size_t slot = (size_t)r + blockIdx.x;
-                    *reinterpret_cast<float4*>(part_acc + (slot * kNumQHeads + head) * kHeadDim + lane * 4) =
-                        make_float4(o0, o1, o2, o3);
-                    if (lane == 0) part_ml[slot * kNumQHeads + head] = make_float2(M, L);
-                }
-            }
-        }
-        named_bar(1 + h, 64);
-        // The whole CTA agrees on abort before anyone leaves the loop (every warp walks the
-        // same segments, so every warp reaches these barriers).
-        if (pair_aborted && (warp & 1) == 0 && lane == 0) S.cta_abort = 1;
-        __syncthreads();
-        const bool cta_aborted = S.cta_abort != 0;
-        if (!whole && !cta_aborted) {
-            // Split row: count this CTA's partial in; the CTA that completes the count
-            // merges all of the row's partials (their writes are published by the fence
-            // before the count, and read past L1 after it).
-            if (threadIdx.x == 0) {
+        if (!whole) {
+            // Split row: once every warp's partial is written, count this CTA's partial
+            // in; the CTA that completes the count merges all of the row's partials
+            // (their writes are published by the fence before the count, and read past
+            // L1 after it).  Every warp walks the same segments (an aborted warp skips
+            // only the work), so every warp reaches these barriers.
+            __syncthreads();
+            const bool cta_aborted = S.cta_abort != 0;
+            if (!cta_aborted && threadIdx.x == 0) {
                 __threadfence();
                 const int c0 = owner_cta(req_lo, P, G), c1 = owner_cta(req_hi - 1, P, G);
                 const int old = atomicAdd(&seg_count[r], 1);
@@ -466,11 +498,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
                 if (S.merge_last) __threadfence();
             }
             __syncthreads();
-            if (S.merge_last) merge_partials(r, row, owner_cta(req_lo, P, G), owner_cta(req_hi - 1, P, G), part_acc,
-                                             part_ml, out);
+            if (!cta_aborted && S.merge_last)
+                merge_partials(r, row, owner_cta(req_lo, P, G), owner_cta(req_hi - 1, P, G), part_acc, part_ml, out);
             __syncthreads();
         }
-        if (cta_aborted) break;
         // next request that has blocks
         ++r;
         while (r + 1 <= num_reqs - 1 && page_off[r + 1] == page_off[r]) ++r;
@@ -510,14 +541,14 @@ int decode_grid(const StepArgs& a, int wave) {
 
 }  // namespace
 
-cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream) {
+cudaError_t launch_decode(const StepArgs& a, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                          cudaStream_t stream) {
     const StepLayout& L = a.lay;
-    const size_t smem = sizeof(DecodeSmem) + 128;
+    const size_t smem = sizeof(DecodeSmem) + 1024;
     const int wave = decode_wave(a);
-    return launch_pdl(decode_kernel, dim3(decode_grid(a, wave)), dim3(kDecThreads), smem, stream,
+    return launch_pdl(decode_kernel, dim3(decode_grid(a, wave)), dim3(kDecThreads), smem, stream, *tmap_k, *tmap_v,
                       static_cast<const __nv_bfloat16*>(a.q), static_cast<__nv_bfloat16*>(a.out), a.cu_seqlens_q,
                       a.context_lens, a.block_tables, a.max_blocks_per_seq, a.num_blocks,
-                      static_cast<const uint8_t*>(a.k_cache), static_cast<const uint8_t*>(a.v_cache),
                       reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs, wave,
                       reinterpret_cast<const int32_t*>(a.ws + L.counters_off),
                       reinterpret_cast<float*>(a.ws + L.part_acc_off), reinterpret_cast<float2*>(a.ws + L.part_ml_off),
@@ -526,7 +557,7 @@ cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream) {
 
 cudaError_t configure_decode_kernel() {
     return cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)(sizeof(DecodeSmem) + 128));
+                                (int)(sizeof(DecodeSmem) + 1024));
 }
 
 }  // namespace kvp

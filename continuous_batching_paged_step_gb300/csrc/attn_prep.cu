@@ -30,23 +30,33 @@ namespace {
 
 constexpr int kPrepThreads = 1024;
 
-// Cost model of the SM split, in units of one key tile of one prefill CTA (128 keys x
-// 64 query tokens x 4 heads through QK^T, softmax and P.V: about 2.2 us on a GB300 SM).
-// A prefill CTA costs its key tiles plus a fixed start/finish; one decode block (64 KiB of
-// K and V) costs a decode CTA about 0.68 units.  Both kinds of work are bound by their
-// SM's own throughput (tensor pipe / issue), so the SMs are shared out in proportion to
-// each side's SM-time, biased a little towards the decode: the prefill can spread over
-// every SM once the decode is done, but a late decode CTA cannot be helped.
+// Cost model of the SM split.  Prefill work is counted in units of one key tile of one
+// prefill CTA (128 keys x 64 query tokens x 4 heads through QK^T, softmax and P.V: about
+// 2.2 us on a GB300 SM), plus a fixed start/finish per CTA.  The decode is HBM-bound: on
+// enough SMs it streams its blocks (64 KiB of K and V each) at about 0.0102 us per block
+// for the whole GPU, and a single SM streams about one block per 0.77 us.  So the decode
+// keeps as many SMs as the prefill leaves it, where the prefill is given enough SMs to
+// finish its work in about the decode's HBM-bound time (its tiles run about 1.5x slower
+// beside a decode that saturates HBM); but never fewer SMs than it needs to finish
+// within the prefill's own time on the whole GPU (x 1.25), up to the 64 SMs that keep
+// HBM near its streaming rate.
+constexpr float kUnitUs = 2.2f;
 constexpr float kTileFixedUnits = 2.f;
-constexpr float kDecodeUnitsPerBlock = 0.68f;
-constexpr float kPrefillShareBias = 0.92f;
+constexpr float kDecodeBlockUsGpu = 0.0102f;
+constexpr float kDecodeBlockUsSm = 0.77f;
+constexpr float kPrefillBesideDecode = 1.5f;
+constexpr float kDecodeMargin = 1.25f;
+constexpr int kDecodeHbmSms = 64;
 
 // Decode CTAs for P decode blocks next to prefill work w (units) on n SMs.
 __device__ int decode_sm_share(int P, float w, int n) {
     if (P <= 0 || w <= 0.f || n < 2) return n;
-    const float d = P * kDecodeUnitsPerBlock;
-    const int s = (int)(n * kPrefillShareBias * w / (w + d));
-    return max(1, min(n, n - s));
+    const float prefill_us = w * kUnitUs;                       // SM-microseconds
+    const float decode_us = P * kDecodeBlockUsGpu;              // on the whole GPU
+    const float n_p = ceilf(kPrefillBesideDecode * prefill_us / decode_us);
+    const float lo = fminf(ceilf(kDecodeMargin * P * kDecodeBlockUsSm * n / prefill_us), (float)kDecodeHbmSms);
+    const float d = fmaxf(lo, (float)n - n_p);
+    return max(1, min(n - 1, (int)d));
 }
 
 __device__ __forceinline__ int2 warp_incl_scan(int2 v, int lane) {

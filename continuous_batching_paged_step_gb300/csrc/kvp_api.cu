@@ -36,8 +36,10 @@ struct kvp_pool {
     int32_t* h_stage[2] = {nullptr, nullptr};  // pinned staging for refcount uploads
     cudaEvent_t stage_ev[2] = {nullptr, nullptr};
     int stage_next = 0;
-    CUtensorMap tmap_k;
+    CUtensorMap tmap_k;       // (block, head) tiles: boxes of 16 rows (prefill)
     CUtensorMap tmap_v;
+    CUtensorMap tmap_k_blk;   // whole blocks: boxes of 128 rows (decode)
+    CUtensorMap tmap_v_blk;
     // diagnostics
     long long launches = 0;
     std::vector<cudaEvent_t> t_events;  // 2 per timed launch
@@ -74,13 +76,13 @@ void mark_dirty(kvp_pool* p, int id) {
 }
 
 // K or V pool viewed as rows of 128 bf16: row (b * 8 + h) * 16 + slot; boxes of 64 dims x
-// 16 rows (one (block, head) tile half), 128-byte swizzle.
-bool encode_pool_map(CUtensorMap* m, void* base, int num_blocks) {
+// box_rows rows (16: one (block, head) tile half; 128: one block's half), 128-byte swizzle.
+bool encode_pool_map(CUtensorMap* m, void* base, int num_blocks, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)kvp::kHeadDim, (cuuint64_t)num_blocks * kvp::kNumKvHeads * kvp::kBlockSize};
     const cuuint64_t strides[1] = {(cuuint64_t)kvp::kHeadBytes};
-    const cuuint32_t box[2] = {64, (cuuint32_t)kvp::kBlockSize};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     const cuuint32_t es[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -143,8 +145,11 @@ kvp_status ensure_device(kvp_pool* p) {
                  cudaSuccess &&
              cudaEventCreateWithFlags(&p->stage_ev[i], cudaEventDisableTiming) == cudaSuccess;
     ok = ok && kvp::configure_decode_kernel() == cudaSuccess && kvp::configure_prefill_kernel() == cudaSuccess;
-    ok = ok && encode_pool_map(&p->tmap_k, p->k_cache, p->num_blocks) &&
-         encode_pool_map(&p->tmap_v, p->v_cache, p->num_blocks);
+    const int tile_rows = kvp::kBlockSize, block_rows = kvp::kBlockSize * kvp::kNumKvHeads;
+    ok = ok && encode_pool_map(&p->tmap_k, p->k_cache, p->num_blocks, tile_rows) &&
+         encode_pool_map(&p->tmap_v, p->v_cache, p->num_blocks, tile_rows) &&
+         encode_pool_map(&p->tmap_k_blk, p->k_cache, p->num_blocks, block_rows) &&
+         encode_pool_map(&p->tmap_v_blk, p->v_cache, p->num_blocks, block_rows);
     if (!ok) {
         release_device(p);
         return KVP_E_CUDA;
@@ -494,7 +499,7 @@ kvp_status paged_attention_step(kvp_pool* p, const void* q, void* out, const int
         return KVP_E_CUDA;
     // decode first; the prefill kernel follows as its programmatic dependent and runs on
     // the SMs the decode leaves free (the metadata kernel sizes the split)
-    if (timed_launch(p, KVP_KERNEL_DECODE, s, [&] { return kvp::launch_decode(a, s); }) != cudaSuccess)
+    if (timed_launch(p, KVP_KERNEL_DECODE, s, [&] { return kvp::launch_decode(a, &p->tmap_k_blk, &p->tmap_v_blk, s); }) != cudaSuccess)
         return KVP_E_CUDA;
     if (max_q_len >= 2 && lay.max_prefill_tiles > 0) {
         CUtensorMap tq;

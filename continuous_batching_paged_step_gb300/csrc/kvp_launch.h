@@ -59,7 +59,8 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t
                              cudaStream_t stream);
 
 cudaError_t launch_step_prep(const StepArgs& a, cudaStream_t stream);
-cudaError_t launch_decode(const StepArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const StepArgs& a, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                          cudaStream_t stream);
 cudaError_t launch_prefill(const StepArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
                            const CUtensorMap* tmap_v, cudaStream_t stream);
 
