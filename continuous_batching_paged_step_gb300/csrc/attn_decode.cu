@@ -6,40 +6,42 @@
 // Decode streams the whole KV history every step (same page, section "为什么 decode 是
 // bandwidth-bound"), so the kernel is built to keep HBM busy:
 //
-// * Balanced split: the 16-token blocks of all decode rows, concatenated in request
-//   order (page_off[r] = first global block of request r), are cut into equal contiguous
+// * Work: the 16-token blocks of all decode rows, concatenated in request order
+//   (page_off[r] = first global block of request r), are cut into equal contiguous
 //   ranges, one per CTA (one CTA per SM of the decode's share of the SMs, which the step's
 //   metadata kernel sizes so that the prefill tiles run on the others; fewer CTAs when
 //   there are under 4 blocks per CTA; more, in whole waves, when a range would exceed the
-//   2,048 block ids a CTA stages).  A CTA walks its range request by request; a request
-//   cut by a range boundary produces one partial per CTA that touches it (slot r + cta),
-//   merged by whichever of those CTAs finishes last; a request inside one range is
+//   1,024 blocks a CTA stages).  SMs do not all get the same share of HBM bandwidth (on
+//   a GB300 some SMs finish equal ranges up to ~20 % later, the same SMs every step), so
+//   each range keeps only its first 80 % as the CTA's own part; its last 20 % is cut into
+//   a few chunks that any CTA takes, through one global counter, once its own part is
+//   issued.  Fast SMs so take more chunks and all CTAs end together.
+// * Pieces (own parts and chunks) are numbered densely in sequence order.  A request cut
+//   by piece boundaries produces one partial per piece and KV head (slot r + piece); the
+//   last warp to finish a (request, KV head) merges them; a request inside one piece is
 //   finished in place.
-// * The CTA first looks up the physical ids of all its blocks in parallel (into shared
-//   memory), so no table lookup sits between a freed buffer and its refill.
-// * One block of all 8 KV heads is 128 rows (head x token) of 128 dims in the pool, so
-//   its K and its V arrive with four tensor-map loads (one per 64-dim half, 128-byte
-//   swizzle) into a 3-stage ring of 64 KiB stages; the last of the 8 warps to finish
-//   with a stage refills it with the block three ahead (no thread waits for the others
-//   to do so).
-// * One warp per KV head.  Its 4 query heads share every K/V byte (GQA packing), and the
-//   two contractions of a block are small matrix products, which run on the tensor
-//   cores (mma.sync m16n8k16, bf16 operands, fp32 accumulation) instead of as thousands
-//   of scalar FMAs:  S^T = K Q^T (16 tokens x 8 columns, the 4 query heads and 4 zero
-//   columns) and O^T += V^T P^T (128 dims x 8 columns).  K and V fragments come from
-//   the swizzled tiles with ldmatrix (V transposed on the way), so reads are free of
-//   bank conflicts; the weights go from the score fragment to the P^T operand with one
-//   register transpose (movmatrix) per 8 tokens.
+// * One producer warp per CTA issues all copies: the block ids, requests and positions
+//   of the own part are looked up by the whole CTA up front (into shared memory), those
+//   of a chunk by a scheduler warp, which claims the chunk when the producer asks (a few
+//   blocks before it runs out of work) while earlier blocks stream.  One block of all 8 KV heads is 128 rows (head x token) of 128 dims in the
+//   pool, so its K and its V arrive with four tensor-map loads (one per 64-dim half,
+//   128-byte swizzle) into a 3-stage ring of 64 KiB stages; with each stage the producer
+//   hands the consumers the block's request, position and segment flags.
+// * One consumer warp per KV head.  Its 4 query heads share every K/V byte (GQA
+//   packing), and the two contractions of a block are small matrix products, which run
+//   on the tensor cores (mma.sync m16n8k16, bf16 operands, fp32 accumulation) instead
+//   of as thousands of scalar FMAs:  S^T = K Q^T (16 tokens x 8 columns, the 4 query
+//   heads and 4 zero columns) and O^T += V^T P^T (128 dims x 8 columns).  K and V
+//   fragments come from the swizzled tiles with ldmatrix (V transposed on the way), so
+//   reads are free of bank conflicts; the weights go from the score fragment to the
+//   P^T operand with one register transpose (movmatrix) per 8 tokens.  A warp reads all
+//   of its fragments of a block first and releases the stage at once.
 // * Online softmax in base 2 (scores x softmax_scale x log2 e) against a reference max
 //   per head that moves only when a score exceeds it by more than 2^8 (a warp vote; the
 //   max reduction and the rescale run only then), with per-lane partial sums reduced
-//   once per request segment.  Weights enter P.V rounded to bf16; the sums use them
-//   unrounded.
-// Partial results keep (m, l, unnormalised acc); the last CTA to finish a split row
-// (an arrival count per row) merges them: O = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M)
-// l_s with M = max_s m_s.
-// A warp reads all of its K and V fragments of a block into registers before anything
-// else and releases the stage at once, so a stage is held only for those reads.
+//   once per segment.  Weights enter P.V rounded to bf16; the sums use them unrounded.
+// Partial results keep (m, l, unnormalised acc); the merge computes
+// O = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s with M = max_s m_s.
 // Keys at positions >= ctx + 1 of the last block are excluded: score -inf, and their V
 // values zeroed in the fragments (stale bytes could hold NaN, and 0 x NaN is NaN).
 #include <cuda.h>
@@ -51,26 +53,50 @@ namespace kvp {
 
 namespace {
 
-constexpr int kDecWarps = kNumKvHeads;   // one warp per KV head
-constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kConsumerWarps = kNumKvHeads;   // one per KV head
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kSchedulerWarp = kConsumerWarps + 1;
+constexpr int kDecThreads = (kConsumerWarps + 2) * 32;   // + the producer and the scheduler warp
 constexpr int kDecStages = 3;
 constexpr int kBlockRows = kNumKvHeads * kBlockSize;   // rows (head, token) of one block: 128
 constexpr int kHalfTile = kBlockRows * 128;            // one block's 64-dim half: 128 rows x 128 B
 constexpr int kStageBytes = 4 * kHalfTile;             // K and V, two halves each: 64 KiB
 
-constexpr int kIdCap = 2048;   // block ids a CTA stages in shared memory (its whole range)
+constexpr int kIdCap = 1024;       // blocks of a CTA's range (its own part is staged up front)
+constexpr int kTailPercent = 20;   // share of each range handed out as chunks
+constexpr int kChunkTarget = 4;    // blocks per chunk, at least
+constexpr int kMaxPieces = 8;      // pieces per range: own part + chunks
+constexpr int kMaxChunk = 32;      // blocks per chunk, at most (one scheduler lane each)
+constexpr int kClaimLead = 8;      // blocks of the own part still to issue when the first chunk is claimed
+
+// segment flags next to a block's position in its request
+constexpr uint32_t kPosMask = 0x00FFFFFFu;
+constexpr uint32_t kFirst = 1u << 24;   // first block of a segment (request x piece)
+constexpr uint32_t kLast = 1u << 25;    // last block of a segment
+constexpr uint32_t kWhole = 1u << 26;   // the segment is the whole request
+
+// What a consumer needs to know about a block besides its K/V.
+struct BlockInfo {
+    int id;        // physical block
+    int r;         // request (-1: no more blocks)
+    int row;       // the request's packed row (query and output)
+    int n_keys;    // ctx + 1
+    uint32_t posf; // block index within the request | segment flags
+};
 
 struct __align__(1024) DecodeSmem {
     uint8_t kv[kDecStages][2][2][kHalfTile];   // [stage][K|V][dim half][row 16 h + token], 128-byte swizzle
-    int32_t ids[kIdCap];                       // physical block of each block of the range
-    int cta_abort;
-    int merge_last;
+    BlockInfo own[kIdCap];                      // the CTA's own part
+    BlockInfo chunk[2][kMaxChunk];              // chunks taken from the pool (double-buffered)
+    BlockInfo meta[kDecStages];                 // block in each stage
+    int piece[kDecStages];
+    int chunk_n[2], chunk_piece[2];             // blocks (0: the pool is empty) and piece of each chunk buffer
     int first_req, last_req;
-    unsigned released[kDecStages];             // warps done with a stage (mod 8)
-    int issued;                                // blocks issued so far
-    int n_rel;                                 // blocks in the range
+    int stop;                                   // the producer asks the scheduler to leave
     uint64_t policy;
-    uint64_t full[kDecStages];
+    uint64_t full[kDecStages], empty[kDecStages];
+    uint64_t req;                               // producer -> scheduler: claim the next chunk
+    uint64_t rdy[2];                            // scheduler -> producer: chunk buffer filled
 };
 
 // Tensor-map load with an L2 eviction hint.
@@ -112,42 +138,6 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
     return y;
 }
 
-// Copy K and V of block `q` of the range into stage `st`.
-__device__ __forceinline__ void issue_block(DecodeSmem& S, const CUtensorMap* tk, const CUtensorMap* tv, int st,
-                                            int q) {
-    const int y = S.ids[q] * kBlockRows;
-    const uint32_t bar = smem_u32(&S.full[st]);
-    const uint32_t d = smem_u32(S.kv[st][0][0]);
-    mbar_arrive_expect_tx(&S.full[st], kStageBytes);
-    tma_load_2d_hint(d, tk, 0, y, bar, S.policy);
-    tma_load_2d_hint(d + kHalfTile, tk, 64, y, bar, S.policy);
-    tma_load_2d_hint(d + 2 * kHalfTile, tv, 0, y, bar, S.policy);
-    tma_load_2d_hint(d + 3 * kHalfTile, tv, 64, y, bar, S.policy);
-    atomicMax(&S.issued, q + 1);
-}
-
-// atom.add with acquire-release ordering at CTA scope (shared memory).
-__device__ __forceinline__ unsigned atomic_add_acq_rel_cta(unsigned* p, unsigned v) {
-    unsigned old;
-    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
-    return old;
-}
-
-// Lane 0 of a warp that is done reading block `rel` (stage st; the warp's reads are
-// ordered before this by __syncwarp): the last of the 8 warps refills the stage with
-// block rel + kDecStages.  One shared atomic per warp and block: the count both elects
-// the refilling warp and orders every warp's accesses (release) before the copy
-// (acquire, then a proxy fence for the tensor copy's write).
-__device__ __forceinline__ void release_stage(DecodeSmem& S, const CUtensorMap* tk, const CUtensorMap* tv, int st,
-                                              int rel) {
-    const unsigned old = atomic_add_acq_rel_cta(&S.released[st], 1u);
-    if ((old & (kDecWarps - 1)) != kDecWarps - 1) return;
-    const int q = rel + kDecStages;
-    if (q >= S.n_rel) return;
-    fence_proxy_async_smem();
-    issue_block(S, tk, tv, st, q);
-}
-
 // A decode CTA streams at least this many blocks: with fewer blocks than CTAs x this,
 // only ceil(P / kMinBlocksPerCta) CTAs take part (fewer, longer segments to merge).
 constexpr int kMinBlocksPerCta = 4;
@@ -172,136 +162,257 @@ __device__ __forceinline__ int owner_cta(int x, int P, int G) {
     return (int)((((long long)x + 1) * G - 1) / P);
 }
 
+// How the P blocks are cut: G ranges of pp pieces each, the own part (piece 0 of a
+// range) and pp - 1 chunks of its tail.  pp is the same for every range (so pieces
+// number densely) and at most kMaxDecodeCtas / G (so r + piece stays inside the
+// workspace's num_reqs + kMaxDecodeCtas partial slots).
+struct Layout {
+    int P, G, pp;
+};
 
-// Merge the partial results of a decode row whose blocks were split over CTAs c0..c1
-// (all 256 threads of the CTA: thread t takes query head t / 8 and dims 16 (t % 8) ..
-// 16 (t % 8) + 15).  O = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c.
-__device__ __noinline__ void merge_partials(int r, int row, int c0, int c1, const float* part_acc,
-                                            const float2* part_ml, __nv_bfloat16* out) {
-    const int head = threadIdx.x >> 3, d0 = (threadIdx.x & 7) * 16;
-    float M = -INFINITY;
-    for (int c = c0; c <= c1; ++c) M = fmaxf(M, __ldcg(&part_ml[((size_t)r + c) * kNumQHeads + head]).x);
-    const float Mu = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f, o[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) o[i] = 0.f;
-    for (int c = c0; c <= c1; ++c) {
-        const size_t sh = ((size_t)r + c) * kNumQHeads + head;
-        const float2 ml = __ldcg(&part_ml[sh]);
-        const float w = fast_exp2(ml.x - Mu);
-        L = fmaf(ml.y, w, L);
-        const float4* src = reinterpret_cast<const float4*>(part_acc + sh * kHeadDim + d0);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float4 a = __ldcg(src + j);
-            o[4 * j + 0] = fmaf(a.x, w, o[4 * j + 0]);
-            o[4 * j + 1] = fmaf(a.y, w, o[4 * j + 1]);
-            o[4 * j + 2] = fmaf(a.z, w, o[4 * j + 2]);
-            o[4 * j + 3] = fmaf(a.w, w, o[4 * j + 3]);
-        }
+__device__ __forceinline__ Layout make_layout(int P, int G) {
+    Layout L{P, G, 1};
+    const int n_min = P / G;   // the shortest range
+    const int n_ch = min(min(kMaxPieces, kMaxDecodeCtas / G) - 1, n_min * kTailPercent / 100 / kChunkTarget);
+    if (n_ch >= 1) L.pp = 1 + n_ch;
+    return L;
+}
+
+// Tail of a range of n blocks: >= pp - 1 when pp > 1, so that no chunk is empty, and at
+// most kMaxChunk blocks per chunk.
+__device__ __forceinline__ int tail_blocks(const Layout& L, int n) {
+    return L.pp > 1 ? min(n * kTailPercent / 100, (L.pp - 1) * kMaxChunk) : 0;
+}
+
+// Global blocks [s, e) of piece pi.
+__device__ __forceinline__ void piece_bounds(const Layout& L, int pi, int& s, int& e) {
+    const int c = pi / L.pp, j = pi % L.pp;
+    int lo, hi;
+    cta_range(L.P, c, L.G, lo, hi);
+    const int tail = tail_blocks(L, hi - lo), mid = hi - tail;
+    if (j == 0) {
+        s = lo;
+        e = mid;
+        return;
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * kQRowElems + head * kHeadDim + d0);
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        uint4 wv;
-        wv.x = pack_bf16x2(o[8 * j + 0] * inv, o[8 * j + 1] * inv);
-        wv.y = pack_bf16x2(o[8 * j + 2] * inv, o[8 * j + 3] * inv);
-        wv.z = pack_bf16x2(o[8 * j + 4] * inv, o[8 * j + 5] * inv);
-        wv.w = pack_bf16x2(o[8 * j + 6] * inv, o[8 * j + 7] * inv);
-        dst[j] = wv;
+    const int n_ch = L.pp - 1;
+    s = mid + (int)((long long)tail * (j - 1) / n_ch);
+    e = mid + (int)((long long)tail * j / n_ch);
+}
+
+// The piece holding global block x.
+__device__ __forceinline__ int piece_of(const Layout& L, int x) {
+    const int c = owner_cta(x, L.P, L.G);
+    int lo, hi;
+    cta_range(L.P, c, L.G, lo, hi);
+    const int tail = tail_blocks(L, hi - lo), mid = hi - tail;
+    if (x < mid) return c * L.pp;
+    const int n_ch = L.pp - 1;
+    return c * L.pp + 1 + (int)(((long long)(x - mid + 1) * n_ch - 1) / tail);
+}
+
+// The largest r in [r_lo, num_reqs) with page_off[r] <= x (page_off[r_lo] <= x): the
+// request that owns global block x (requests without decode blocks have empty ranges).
+__device__ __forceinline__ int request_of(const int32_t* page_off, int num_reqs, int r_lo, int x) {
+    int a = r_lo, step = 1;
+    while (a + step < num_reqs && page_off[a + step] <= x) {
+        a += step;
+        step <<= 1;
     }
+    int b = min(a + step - 1, num_reqs - 1);
+    while (a < b) {
+        const int mid = (a + b + 1) >> 1;
+        if (page_off[mid] <= x) a = mid;
+        else b = mid - 1;
+    }
+    return a;
+}
+
+// Everything a consumer needs about global block x of request r, in piece [s, e).
+__device__ __forceinline__ BlockInfo block_info(int x, int r, int s, int e, const int32_t* page_off,
+                                                const int32_t* tables, int max_blocks, int num_blocks,
+                                                const int32_t* cu, const int32_t* ctx, uint32_t* err) {
+    BlockInfo b;
+    const int a0 = page_off[r], a1 = page_off[r + 1];
+    const int pos = x - a0;
+    int id = tables[(size_t)r * max_blocks + pos];
+    if ((unsigned)id >= (unsigned)num_blocks) {
+        raise_error(err, kErrBadBlock);
+        id = 0;
+    }
+    b.id = id;
+    b.r = r;
+    b.row = cu[r];
+    b.n_keys = ctx[r] + 1;
+    b.posf = (uint32_t)pos | ((x == s || x == a0) ? kFirst : 0u) | ((x == e - 1 || x == a1 - 1) ? kLast : 0u) |
+             ((a0 >= s && a1 <= e) ? kWhole : 0u);
+    return b;
 }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-__global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
-    const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-    const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ out, const int32_t* __restrict__ cu,
-    const int32_t* __restrict__ ctx, const int32_t* __restrict__ tables, int max_blocks, int num_blocks,
-    const int32_t* __restrict__ page_off, int num_reqs, int wave, const int32_t* __restrict__ counters,
-    float* __restrict__ part_acc, float2* __restrict__ part_ml, int32_t* __restrict__ seg_count, float scale_log2,
-    uint32_t* __restrict__ err) {
-    extern __shared__ uint8_t smem_raw[];
-    DecodeSmem& S =
-        *reinterpret_cast<DecodeSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        prefetch_tmap(&tmap_k);
-        prefetch_tmap(&tmap_v);
-    }
-    grid_dep_wait();     // block offsets, cache contents
-    grid_dep_launch();
-    const int P = page_off[num_reqs];
-    if (P <= 0) return;
-    // SMs left to this step's prefill tiles run them meanwhile (unless the launch is too
-    // small for the narrower waves that would need)
-    int G = decode_ctas_used(P, max(1, min(wave, counters[2])), gridDim.x);
-    if (G == 0) G = decode_ctas_used(P, wave, gridDim.x);
-    if (G == 0) {
-        // the launch has too few CTAs for this many blocks (the host sizes it from an
-        // upper bound, so this means inconsistent metadata)
-        if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(err, kErrBadMeta);
-        return;
-    }
-    if ((int)blockIdx.x >= G) return;
-    int lo, hi;
-    cta_range(P, blockIdx.x, G, lo, hi);
-    if (lo >= hi) return;
-    const int n_rel = hi - lo;   // <= kIdCap by construction of G
-    if (n_rel > kIdCap) {
-        if (threadIdx.x == 0) raise_error(err, kErrBadMeta);
-        return;
-    }
+struct DecodeArgs {
+    const __nv_bfloat16* q;
+    __nv_bfloat16* out;
+    const int32_t* cu;
+    const int32_t* ctx;
+    const int32_t* tables;
+    int max_blocks;
+    int num_blocks;
+    const int32_t* page_off;
+    int num_reqs;
+    int wave;
+    int32_t* counters;   // [2]: decode CTAs wanted, [4]: chunks taken
+    float* part_acc;
+    float2* part_ml;
+    float scale_log2;
+    uint32_t* err;
+};
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kDecStages; ++s) {
-            mbar_init(&S.full[s], 1);
-            S.released[s] = 0;
+// The scheduler warp: on each request of the producer, claims the next chunk from the
+// pool (one global counter) and describes its blocks into chunk buffer i % 2 (the
+// producer has finished issuing the chunk that buffer held before).  Leaves after handing
+// over an empty chunk, or when the producer asks it to.
+__device__ __forceinline__ void schedule(DecodeSmem& S, const DecodeArgs& a, const Layout& L, int lane) {
+    const int n_chunks = L.G * (L.pp - 1);
+    for (int i = 0;; ++i) {
+        if (!warp_wait(&S.req, (uint32_t)(i & 1))) {
+            if (lane == 0) raise_error(a.err, kErrTimeout);
+            return;
         }
-        S.issued = 0;
-        S.n_rel = n_rel;
-        S.policy = policy_evict_first();
-        S.cta_abort = 0;
-        fence_barrier_init();
-    }
-    // requests holding the first and the last block of the range (one parallel pass)
-    for (int r = threadIdx.x; r < num_reqs; r += kDecThreads) {
-        const int a0 = page_off[r], a1 = page_off[r + 1];
-        if (a0 <= lo && lo < a1) S.first_req = r;
-        if (a0 <= hi - 1 && hi - 1 < a1) S.last_req = r;
-    }
-    __syncthreads();
-    // physical id of every block of the range
-    {
-        const int r_first = S.first_req, r_last = S.last_req;
-        for (int x = lo + threadIdx.x; x < hi; x += kDecThreads) {
-            int ra = r_first, rb = r_last;   // largest r with page_off[r] <= x
+        if (*(volatile int*)&S.stop) return;
+        const int buf = i & 1;
+        int kk = 0;
+        if (lane == 0) kk = atomicAdd(&a.counters[4], 1);
+        kk = __shfl_sync(0xffffffffu, kk, 0);
+        int n = 0, piece = 0;
+        if (kk < n_chunks) {
+            piece = (kk % L.G) * L.pp + 1 + kk / L.G;
+            int s, e;
+            piece_bounds(L, piece, s, e);
+            // request of block s: a 32-way search over page_off, then each lane its own block
+            int ra = 0, rb = a.num_reqs - 1;
             while (ra < rb) {
-                const int mid = (ra + rb + 1) >> 1;
-                if (page_off[mid] <= x) ra = mid;
-                else rb = mid - 1;
+                const int step = (rb - ra + 32) / 32;
+                const int idx = ra + lane * step;
+                const unsigned m = __ballot_sync(0xffffffffu, idx <= rb && a.page_off[idx] <= s);
+                ra += (31 - __clz(m)) * step;
+                rb = min(rb, ra + step - 1);
             }
-            int b = tables[(size_t)ra * max_blocks + (x - page_off[ra])];
-            if ((unsigned)b >= (unsigned)num_blocks) {
-                raise_error(err, kErrBadBlock);
-                b = 0;
+            n = min(e - s, kMaxChunk);
+            if (lane < n) {
+                const int x = s + lane;
+                const int r = request_of(a.page_off, a.num_reqs, ra, x);
+                S.chunk[buf][lane] =
+                    block_info(x, r, s, e, a.page_off, a.tables, a.max_blocks, a.num_blocks, a.cu, a.ctx, a.err);
             }
-            S.ids[x - lo] = b;
+        }
+        __syncwarp();
+        if (lane == 0) {
+            S.chunk_n[buf] = n;
+            S.chunk_piece[buf] = piece;
+            mbar_arrive(&S.rdy[buf]);   // release: the lanes' descriptions are ordered by the __syncwarp
+        }
+        if (n == 0) return;
+    }
+}
+
+// The producer warp: issues the CTA's own part, then the chunks the scheduler claims,
+// one block per free stage; ends with a stage that carries r = -1.  It asks for the next
+// chunk kClaimLead blocks before the end of the own part and at the start of each chunk,
+// so that the claim and its table lookups run while earlier blocks stream.
+__device__ __forceinline__ void produce(DecodeSmem& S, const DecodeArgs& a, const CUtensorMap* tk,
+                                        const CUtensorMap* tv, const Layout& L, int n_own, int lane) {
+    int k = 0;   // blocks issued
+    bool ok = true;
+    // lane 0: wait for stage k % kDecStages to be free, describe the block, copy it
+    auto issue = [&](const BlockInfo& b, int piece) -> bool {
+        const int st = k % kDecStages;
+        if (!mbar_wait(&S.empty[st], ((k / kDecStages) & 1) ^ 1)) return false;
+        S.meta[st] = b;
+        S.piece[st] = piece;
+        const int y = b.id * kBlockRows;
+        const uint32_t bar = smem_u32(&S.full[st]);
+        const uint32_t d = smem_u32(S.kv[st][0][0]);
+        mbar_arrive_expect_tx(&S.full[st], kStageBytes);
+        tma_load_2d_hint(d, tk, 0, y, bar, S.policy);
+        tma_load_2d_hint(d + kHalfTile, tk, 64, y, bar, S.policy);
+        tma_load_2d_hint(d + 2 * kHalfTile, tv, 0, y, bar, S.policy);
+        tma_load_2d_hint(d + 3 * kHalfTile, tv, 64, y, bar, S.policy);
+        return true;
+    };
+    int n_req = 0, n_got = 0;   // chunks asked for, chunks received
+    auto request = [&]() {
+        if (lane == 0) mbar_arrive(&S.req);
+        ++n_req;
+    };
+    // whole warp: the next chunk's blocks (0: the pool is empty, -1: the wait ran out)
+    auto receive = [&](int& buf, int& piece) -> int {
+        buf = n_got & 1;
+        const bool w = warp_wait(&S.rdy[buf], (uint32_t)((n_got >> 1) & 1));
+        ++n_got;
+        if (!w) return -1;
+        piece = S.chunk_piece[buf];
+        return S.chunk_n[buf];
+    };
+
+    const bool pool = L.pp > 1;
+    const int own_piece = (int)blockIdx.x * L.pp;
+    const int claim_at = max(0, n_own - kClaimLead);
+    for (int q = 0; q < n_own && ok; ++q) {
+        if (q == claim_at && pool) request();
+        if (lane == 0) ok = issue(S.own[q], own_piece);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        ++k;
+    }
+    int n = 0, buf = 0, piece = 0;
+    bool sched_done = !pool;   // the scheduler has handed over an empty chunk and left
+    if (ok && pool) n = receive(buf, piece);
+    while (ok && n > 0) {
+        request();   // the chunk after this one, into the other buffer
+        for (int q = 0; q < n && ok; ++q) {
+            if (lane == 0) ok = issue(S.chunk[buf][q], piece);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            ++k;
+        }
+        if (ok) n = receive(buf, piece);
+    }
+    if (n < 0) ok = false;
+    if (ok && pool) sched_done = true;   // the loop ended on n == 0
+    if (lane == 0) {
+        if (!sched_done && n_req == n_got) {
+            // stopped early (an error) with no claim outstanding: let the scheduler go
+            *(volatile int*)&S.stop = 1;
+            mbar_arrive(&S.req);
+        }
+        bool ended = false;
+        if (ok) {
+            // no more blocks: a stage without a copy, r = -1
+            const int st = k % kDecStages;
+            if (mbar_wait(&S.empty[st], ((k / kDecStages) & 1) ^ 1)) {
+                S.meta[st].r = -1;
+                mbar_arrive(&S.full[st]);
+                ended = true;
+            }
+        }
+        if (!ok || !ended) raise_error(a.err, kErrTimeout);
+        // The CTA must not retire while a copy still targets its shared memory: wait for
+        // the last blocks issued into each stage (the stage of the end marker was seen
+        // consumed already).
+        for (int j = max(0, k - kDecStages); j < k; ++j) {
+            if (ended && j % kDecStages == k % kDecStages) continue;
+            if (!mbar_wait(&S.full[j % kDecStages], (uint32_t)((j / kDecStages) & 1))) raise_error(a.err, kErrTimeout);
         }
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int j = 0; j < kDecStages && j < n_rel; ++j) issue_block(S, &tmap_k, &tmap_v, j, j);
+}
 
-    }
-
+// A consumer warp (KV head h): every block of the CTA's sequence, in stage order.
+__device__ __forceinline__ void consume(DecodeSmem& S, const DecodeArgs& a, const Layout& L, int h, int lane) {
     // Fragment coordinates (PTX mma.m16n8k16 layouts): lane = 4 g + t.  A fragment rows
     // are tokens (S^T) or dims (O^T); B columns and C columns are the query heads, of
     // which columns 0..3 are real (lanes with t < 2 hold them in C).
-    const int h = warp;
     const int g = lane >> 2, t = lane & 3;
     const int x7 = lane & 7;
     // ldmatrix row addresses inside a stage's K (V) region, 64-dim half 0: K row = token
@@ -319,202 +430,352 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(
         }
     }
     const uint32_t ring0 = smem_u32(S.kv[0][0][0]);
-    int stage = 0;
-    uint32_t phase = 0;
-    bool aborted = false;
-
-    int r = S.first_req;
-    int page = lo;
-    while (page < hi) {
-        const int req_lo = page_off[r], req_hi = page_off[r + 1];
-        const int seg_end = min(hi, req_hi);
-        const bool whole = (page == req_lo) && (seg_end == req_hi);
-        const int row = cu[r];
-        const int n_keys = ctx[r] + 1;
-
-        // Q^T as the B operand of S^T = K Q^T: k-step s covers dims 16 s .. 16 s + 15; lane
-        // (g, t) holds head g's dims 16 s + 2 t, +1 and 16 s + 2 t + 8, +9 (zero for g >= 4)
-        uint32_t qb[8][2];
-        {
-            const uint32_t* qw = reinterpret_cast<const uint32_t*>(q + (size_t)row * kQRowElems +
+    uint32_t qb[8][2];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // heads 2t, 2t + 1
+    float o[8][4];
+    for (int k = 0;; ++k) {
+        const int stage = k % kDecStages;
+        if (!warp_wait(&S.full[stage], (uint32_t)((k / kDecStages) & 1))) {
+            if (lane == 0) raise_error(a.err, kErrTimeout);
+            return;
+        }
+        const BlockInfo b = S.meta[stage];
+        if (b.r < 0) return;
+        const int piece = S.piece[stage];
+        if (b.posf & kFirst) {
+            // Q^T as the B operand of S^T = K Q^T: k-step s covers dims 16 s .. 16 s + 15;
+            // lane (g, t) holds head g's dims 16 s + 2 t, +1 and 16 s + 2 t + 8, +9 (zero
+            // for g >= 4)
+            const uint32_t* qw = reinterpret_cast<const uint32_t*>(a.q + (size_t)b.row * kQRowElems +
                                                                     (h * kGroup + (g & 3)) * kHeadDim);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 qb[s][0] = g < kGroup ? __ldg(qw + 8 * s + t) : 0u;
                 qb[s][1] = g < kGroup ? __ldg(qw + 8 * s + 4 + t) : 0u;
             }
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
         }
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // heads 2t, 2t + 1
-        float o[8][4];
+        const uint32_t kb = ring0 + stage * kStageBytes, vb = kb + 2 * kHalfTile;
+        const int n_valid = b.n_keys - (int)(b.posf & kPosMask) * kBlockSize;   // >= 1; < 16 only in a last block
+        // All of this warp's reads of the stage first (K and V fragments into registers),
+        // then the stage is released, so the refill starts before the arithmetic.
+        uint32_t ka[8][4], va[8][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-
-        for (; page < seg_end; ++page) {
-            if (!aborted && *reinterpret_cast<volatile int*>(&S.cta_abort)) aborted = true;   // another warp gave up
-            if (!aborted && !warp_wait(&S.full[stage], phase)) {
-                if (lane == 0) {
-                    raise_error(err, kErrTimeout);
-                    S.cta_abort = 1;
-                }
-                aborted = true;
-            }
-            if (!aborted) {
-                const uint32_t kb = ring0 + stage * kStageBytes, vb = kb + 2 * kHalfTile;
-                const int n_valid = n_keys - (page - req_lo) * kBlockSize;   // >= 1; < 16 only in a last block
-                // All of this warp's reads of the stage first (K and V fragments into
-                // registers), then the stage is released, so the refill starts before the
-                // arithmetic rather than after it.
-                uint32_t ka[8][4], va[8][4];
+        for (int s = 0; s < 8; ++s) ldsm_x4(kb + (s >> 2) * kHalfTile + k_off[s & 3], ka[s]);
 #pragma unroll
-                for (int s = 0; s < 8; ++s) ldsm_x4(kb + (s >> 2) * kHalfTile + k_off[s & 3], ka[s]);
+        for (int i = 0; i < 8; ++i) ldsm_x4_t(vb + (i >> 2) * kHalfTile + v_off[i & 3], va[i]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[stage]);
+        if (n_valid < kBlockSize) {
+            // tokens past the end of the request: zero their V values (stale bytes could
+            // hold NaN, and 0 x NaN is NaN).  V^T fragment registers 0, 1 hold tokens 2t,
+            // 2t + 1; registers 2, 3 tokens 2t + 8, 2t + 9.
+            auto keep = [&](int tk) -> uint32_t {
+                return (tk < n_valid ? 0x0000FFFFu : 0u) | (tk + 1 < n_valid ? 0xFFFF0000u : 0u);
+            };
+            const uint32_t k01 = keep(2 * t), k89 = keep(2 * t + 8);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) ldsm_x4_t(vb + (i >> 2) * kHalfTile + v_off[i & 3], va[i]);
-                __syncwarp();
-                if (lane == 0) release_stage(S, &tmap_k, &tmap_v, stage, page - lo);
-                if (n_valid < kBlockSize) {
-                    // tokens past the end of the request: zero their V values (stale bytes
-                    // could hold NaN, and 0 x NaN is NaN).  V^T fragment registers 0, 1 hold
-                    // tokens 2t, 2t + 1; registers 2, 3 tokens 2t + 8, 2t + 9.
-                    auto keep = [&](int tk) -> uint32_t {
-                        return (tk < n_valid ? 0x0000FFFFu : 0u) | (tk + 1 < n_valid ? 0xFFFF0000u : 0u);
-                    };
-                    const uint32_t k01 = keep(2 * t), k89 = keep(2 * t + 8);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        va[i][0] &= k01;
-                        va[i][1] &= k01;
-                        va[i][2] &= k89;
-                        va[i][3] &= k89;
-                    }
-                }
-                // ---- S^T = K Q^T: 16 tokens x (4 heads + 4 zero columns)
-                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int s = 0; s < 8; s += 2) {
-                    mma_16816(sa, ka[s], qb[s][0], qb[s][1]);
-                    mma_16816(sb, ka[s + 1], qb[s + 1][0], qb[s + 1][1]);
-                }
-                // lane holds tokens g, g + 8 of heads 2t, 2t + 1: x[0] (g, 2t), x[1] (g, 2t+1),
-                // x[2] (g+8, 2t), x[3] (g+8, 2t+1)
-                float x[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) x[j] = (sa[j] + sb[j]) * scale_log2;
-                if (t >= 2 || g >= n_valid) x[0] = x[1] = -INFINITY;
-                if (t >= 2 || g + 8 >= n_valid) x[2] = x[3] = -INFINITY;
-                // ---- online softmax against the lazily moved reference max
-                const bool need = fmaxf(x[0], x[2]) > m0 + 8.f || fmaxf(x[1], x[3]) > m1 + 8.f;
-                if (__any_sync(0xffffffffu, need)) {
-                    float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
-#pragma unroll
-                    for (int off = 4; off < 32; off <<= 1) {
-                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-                    }
-                    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-                    const float a0 = fast_exp2(m0 - (n0 == -INFINITY ? 0.f : n0));
-                    const float a1 = fast_exp2(m1 - (n1 == -INFINITY ? 0.f : n1));
-                    l0 *= a0;
-                    l1 *= a1;
-                    m0 = n0;
-                    m1 = n1;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        o[i][0] *= a0;
-                        o[i][1] *= a1;
-                        o[i][2] *= a0;
-                        o[i][3] *= a1;
-                    }
-                }
-                const float u0 = m0 == -INFINITY ? 0.f : m0, u1 = m1 == -INFINITY ? 0.f : m1;
-                const float p0 = fast_exp2(x[0] - u0), p1 = fast_exp2(x[1] - u1);
-                const float p2 = fast_exp2(x[2] - u0), p3 = fast_exp2(x[3] - u1);
-                l0 += p0 + p2;
-                l1 += p1 + p3;
-                // P^T as the B operand: lane (g, t) gets head g's weights of tokens 2t, 2t+1
-                // (first 8 tokens) and 2t + 8, 2t + 9 (last 8)
-                const uint32_t pb0 = movmatrix_t(pack_bf16x2(p0, p1));
-                const uint32_t pb1 = movmatrix_t(pack_bf16x2(p2, p3));
-                // ---- O^T += V^T P^T: m-tile i covers dims 16 i .. 16 i + 15
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mma_16816(o[i], va[i], pb0, pb1);
-            }
-            if (++stage == kDecStages) {
-                stage = 0;
-                phase ^= 1;
+            for (int i = 0; i < 8; ++i) {
+                va[i][0] &= k01;
+                va[i][1] &= k01;
+                va[i][2] &= k89;
+                va[i][3] &= k89;
             }
         }
+        // ---- S^T = K Q^T: 16 tokens x (4 heads + 4 zero columns)
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s = 0; s < 8; s += 2) {
+            mma_16816(sa, ka[s], qb[s][0], qb[s][1]);
+            mma_16816(sb, ka[s + 1], qb[s + 1][0], qb[s + 1][1]);
+        }
+        // lane holds tokens g, g + 8 of heads 2t, 2t + 1: x[0] (g, 2t), x[1] (g, 2t+1),
+        // x[2] (g+8, 2t), x[3] (g+8, 2t+1)
+        float x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = (sa[j] + sb[j]) * a.scale_log2;
+        if (t >= 2 || g >= n_valid) x[0] = x[1] = -INFINITY;
+        if (t >= 2 || g + 8 >= n_valid) x[2] = x[3] = -INFINITY;
+        // ---- online softmax against the lazily moved reference max
+        const bool need = fmaxf(x[0], x[2]) > m0 + 8.f || fmaxf(x[1], x[3]) > m1 + 8.f;
+        if (__any_sync(0xffffffffu, need)) {
+            float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+            const float a0 = fast_exp2(m0 - (n0 == -INFINITY ? 0.f : n0));
+            const float a1 = fast_exp2(m1 - (n1 == -INFINITY ? 0.f : n1));
+            l0 *= a0;
+            l1 *= a1;
+            m0 = n0;
+            m1 = n1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                o[i][0] *= a0;
+                o[i][1] *= a1;
+                o[i][2] *= a0;
+                o[i][3] *= a1;
+            }
+        }
+        const float u0 = m0 == -INFINITY ? 0.f : m0, u1 = m1 == -INFINITY ? 0.f : m1;
+        const float p0 = fast_exp2(x[0] - u0), p1 = fast_exp2(x[1] - u1);
+        const float p2 = fast_exp2(x[2] - u0), p3 = fast_exp2(x[3] - u1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+        // P^T as the B operand: lane (g, t) gets head g's weights of tokens 2t, 2t+1
+        // (first 8 tokens) and 2t + 8, 2t + 9 (last 8)
+        const uint32_t pb0 = movmatrix_t(pack_bf16x2(p0, p1));
+        const uint32_t pb1 = movmatrix_t(pack_bf16x2(p2, p3));
+        // ---- O^T += V^T P^T: m-tile i covers dims 16 i .. 16 i + 15
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mma_16816(o[i], va[i], pb0, pb1);
 
-        // ------------------------------------------------ finish the segment
+        if (!(b.posf & kLast)) continue;
+        // ------------------------------------------------ end of a segment
+        float s0 = l0, s1 = l1;
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+            s0 += __shfl_xor_sync(0xffffffffu, s0, off);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, off);
         }
-        if (!aborted) {
-            if (whole) {
-                // O = O^T / l, transposed back so that lane (g, t) holds dims 16 i + 2t, +1
-                // and 16 i + 8 + 2t, +1 of head g
-                const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
-                uint32_t* orow = reinterpret_cast<uint32_t*>(out + (size_t)row * kQRowElems +
-                                                             (h * kGroup + (g & 3)) * kHeadDim);
+        if (b.posf & kWhole) {
+            // O = O^T / l, transposed back so that lane (g, t) holds dims 16 i + 2t, +1
+            // and 16 i + 8 + 2t, +1 of head g
+            const float i0 = s0 > 0.f ? 1.f / s0 : 0.f, i1 = s1 > 0.f ? 1.f / s1 : 0.f;
+            uint32_t* orow = reinterpret_cast<uint32_t*>(a.out + (size_t)b.row * kQRowElems +
+                                                         (h * kGroup + (g & 3)) * kHeadDim);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t w0 = movmatrix_t(pack_bf16x2(o[i][0] * i0, o[i][1] * i1));
-                    const uint32_t w1 = movmatrix_t(pack_bf16x2(o[i][2] * i0, o[i][3] * i1));
-                    if (g < kGroup) {
-                        orow[8 * i + t] = w0;
-                        orow[8 * i + 4 + t] = w1;
-                    }
-                }
-            } else if (t < 2) {
-                const size_t slot = (size_t)r + blockIdx.x;
-                float* pa = part_acc + (slot * kNumQHeads + h * kGroup + 2 * t) * kHeadDim;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    pa[16 * i + g] = o[i][0];
-                    pa[kHeadDim + 16 * i + g] = o[i][1];
-                    pa[16 * i + 8 + g] = o[i][2];
-                    pa[kHeadDim + 16 * i + 8 + g] = o[i][3];
-                }
-                if (g == 0) {
-                    part_ml[slot * kNumQHeads + h * kGroup + 2 * t] = make_float2(m0, l0);
-                    part_ml[slot * kNumQHeads + h * kGroup + 2 * t + 1] = make_float2(m1, l1);
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t w0 = movmatrix_t(pack_bf16x2(o[i][0] * i0, o[i][1] * i1));
+                const uint32_t w1 = movmatrix_t(pack_bf16x2(o[i][2] * i0, o[i][3] * i1));
+                if (g < kGroup) {
+                    orow[8 * i + t] = w0;
+                    orow[8 * i + 4 + t] = w1;
                 }
             }
+            continue;
         }
-        if (!whole) {
-            // Split row: once every warp's partial is written, count this CTA's partial
-            // in; the CTA that completes the count merges all of the row's partials
-            // (their writes are published by the fence before the count, and read past
-            // L1 after it).  Every warp walks the same segments (an aborted warp skips
-            // only the work), so every warp reaches these barriers.
-            __syncthreads();
-            const bool cta_aborted = S.cta_abort != 0;
-            if (!cta_aborted && threadIdx.x == 0) {
-                __threadfence();
-                const int c0 = owner_cta(req_lo, P, G), c1 = owner_cta(req_hi - 1, P, G);
-                const int old = atomicAdd(&seg_count[r], 1);
-                S.merge_last = (old == c1 - c0) ? 1 : 0;
-                if (S.merge_last) __threadfence();
+        // Split row: this piece's partial for the warp's 4 query heads, merged with the
+        // row's other pieces by the combine kernel that follows the step's attention
+        // kernels (so no consumer waits on global memory here).
+        const size_t slot = (size_t)b.r + piece;
+        if (t < 2) {
+            float* pa = a.part_acc + (slot * kNumQHeads + h * kGroup + 2 * t) * kHeadDim;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                pa[16 * i + g] = o[i][0];
+                pa[kHeadDim + 16 * i + g] = o[i][1];
+                pa[16 * i + 8 + g] = o[i][2];
+                pa[kHeadDim + 16 * i + 8 + g] = o[i][3];
             }
-            __syncthreads();
-            if (!cta_aborted && S.merge_last)
-                merge_partials(r, row, owner_cta(req_lo, P, G), owner_cta(req_hi - 1, P, G), part_acc, part_ml, out);
-            __syncthreads();
+            if (g == 0) {
+                a.part_ml[slot * kNumQHeads + h * kGroup + 2 * t] = make_float2(m0, s0);
+                a.part_ml[slot * kNumQHeads + h * kGroup + 2 * t + 1] = make_float2(m1, s1);
+            }
         }
-        // next request that has blocks
-        ++r;
-        while (r + 1 <= num_reqs - 1 && page_off[r + 1] == page_off[r]) ++r;
+    }
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                  const DecodeArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    DecodeSmem& S =
+        *reinterpret_cast<DecodeSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+    }
+    grid_dep_wait();     // block offsets, cache contents
+    grid_dep_launch();
+    const int P = a.page_off[a.num_reqs];
+    if (P <= 0) return;
+    // SMs left to this step's prefill tiles run them meanwhile (unless the launch is too
+    // small for the narrower waves that would need)
+    int G = decode_ctas_used(P, max(1, min(a.wave, a.counters[2])), gridDim.x);
+    if (G == 0) G = decode_ctas_used(P, a.wave, gridDim.x);
+    if (G == 0) {
+        // the launch has too few CTAs for this many blocks (the host sizes it from an
+        // upper bound, so this means inconsistent metadata)
+        if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(a.err, kErrBadMeta);
+        return;
+    }
+    if ((int)blockIdx.x >= G) return;
+    const Layout L = make_layout(P, G);
+    int lo, mid;
+    piece_bounds(L, (int)blockIdx.x * L.pp, lo, mid);   // the own part
+    const int n_own = mid - lo;   // >= 1 and <= kIdCap by construction of G
+    if (n_own < 1 || n_own > kIdCap) {
+        if (threadIdx.x == 0) raise_error(a.err, kErrBadMeta);
+        return;
     }
 
-    // Drain: the CTA must not retire while a copy still targets its shared memory (only
-    // possible after a wait ran out; otherwise every issued block was consumed).
-    __syncthreads();
     if (threadIdx.x == 0) {
-        const int n = S.issued;
-        for (int j = max(0, n - kDecStages); j < n; ++j)
-            if (!mbar_wait(&S.full[j % kDecStages], (uint32_t)((j / kDecStages) & 1))) raise_error(err, kErrTimeout);
+        for (int s = 0; s < kDecStages; ++s) {
+            mbar_init(&S.full[s], 1);
+            mbar_init(&S.empty[s], kConsumerWarps);
+        }
+        mbar_init(&S.req, 1);
+        mbar_init(&S.rdy[0], 1);
+        mbar_init(&S.rdy[1], 1);
+        S.stop = 0;
+        S.policy = policy_evict_first();
+        fence_barrier_init();
     }
+    // requests holding the first and the last block of the own part (one parallel pass)
+    for (int r = threadIdx.x; r < a.num_reqs; r += kDecThreads) {
+        const int a0 = a.page_off[r], a1 = a.page_off[r + 1];
+        if (a0 <= lo && lo < a1) S.first_req = r;
+        if (a0 <= mid - 1 && mid - 1 < a1) S.last_req = r;
+    }
+    __syncthreads();
+    // ids, requests and positions of every block of the own part
+    {
+        const int r_first = S.first_req, r_last = S.last_req;
+        for (int x = lo + threadIdx.x; x < mid; x += kDecThreads) {
+            int ra = r_first, rb = r_last;   // largest r with page_off[r] <= x
+            while (ra < rb) {
+                const int m = (ra + rb + 1) >> 1;
+                if (a.page_off[m] <= x) ra = m;
+                else rb = m - 1;
+            }
+            S.own[x - lo] = block_info(x, ra, lo, mid, a.page_off, a.tables, a.max_blocks, a.num_blocks, a.cu, a.ctx,
+                                       a.err);
+        }
+    }
+    __syncthreads();
+    if (warp == kProducerWarp) produce(S, a, &tmap_k, &tmap_v, L, n_own, lane);
+    else if (warp == kSchedulerWarp) {
+        if (L.pp > 1) schedule(S, a, L, lane);
+    } else consume(S, a, L, warp, lane);
+}
+
+constexpr int kCombineHeads = kNumQHeads / 2;         // query heads of one combine CTA (half a row)
+constexpr int kCombineThreads = kCombineHeads * 32;   // one warp per query head
+constexpr int kCombineStage = 12;                     // pieces staged in shared memory at once
+constexpr int kCombineAccBytes = kCombineHeads * kHeadDim * 4;   // one piece's accumulators: 8 KiB
+constexpr int kCombineMlBytes = kCombineHeads * 8;               // one piece's (m, l): 128 B
+
+constexpr int kCombineRowsPerRound = 32;   // rows a CTA plans at once
+
+struct CombineSmem {
+    float acc[kCombineStage][kCombineHeads][kHeadDim];
+    float2 ml[kCombineStage][kCombineHeads];
+    int4 job[kCombineRowsPerRound];   // {request, row, first piece, last piece} of the rows to merge
+    int n_job;
+    uint64_t full;
+};
+
+// Split-KV combine: every decode row whose blocks the decode kernel cut into several
+// pieces gets O = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p over its pieces
+// (M = max_p m_p), merged online piece by piece.  Two CTAs per row (16 query heads each,
+// one warp per head, lane l holding dims 4l .. 4l + 3); a CTA stages up to kCombineStage
+// pieces' partials at once in shared memory with bulk copies, so a row costs about one
+// round trip to memory.  Rows held by one piece were finished in place.  Launched after
+// the step's attention kernels, as a programmatic dependent: before its wait it works out
+// its row's pieces from the metadata kernel's outputs (complete before the decode kernel
+// let its dependents launch) and the decode launch's size; after the wait (for the decode
+// grid; the prefill grid, when there is one, completes only after it) only the copies and
+// the merge remain.
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const int32_t* __restrict__ page_off, int num_reqs,
+                                                                   const int32_t* __restrict__ cu,
+                                                                   const int32_t* __restrict__ counters,
+                                                                   int decode_wave, int decode_grid,
+                                                                   const float* __restrict__ part_acc,
+                                                                   const float2* __restrict__ part_ml,
+                                                                   __nv_bfloat16* __restrict__ out,
+                                                                   uint32_t* __restrict__ err) {
+    extern __shared__ uint8_t smem_raw[];
+    CombineSmem& S = *reinterpret_cast<CombineSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const int half = blockIdx.x & 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int head = half * kCombineHeads + warp;
+    uint32_t phase = 0;
+    if (threadIdx.x == 0) {
+        mbar_init(&S.full, 1);
+        fence_barrier_init();
+    }
+    // This CTA pair takes rows blockIdx.x / 2 + k * stride; it plans up to
+    // kCombineRowsPerRound of them at once (one thread each), then merges those to merge.
+    const int stride = gridDim.x >> 1;
+    for (int r0 = blockIdx.x >> 1; r0 < num_reqs; r0 += kCombineRowsPerRound * stride) {
+        if (threadIdx.x == 0) S.n_job = 0;
+        __syncthreads();
+        const int r = r0 + (int)threadIdx.x * stride;
+        if (threadIdx.x < kCombineRowsPerRound && r < num_reqs) {
+            // every load at once, then the arithmetic
+            const int P = page_off[num_reqs], want = counters[2];
+            const int a0 = page_off[r], a1 = page_off[r + 1], row = cu[r];
+            int G = 0;   // the decode kernel's CTA count, as it works it out
+            if (P > 0) {
+                G = decode_ctas_used(P, max(1, min(decode_wave, want)), decode_grid);
+                if (G == 0) G = decode_ctas_used(P, decode_wave, decode_grid);
+            }
+            if (G > 0 && a1 > a0) {   // a decode row
+                const Layout L = make_layout(P, G);
+                const int p0 = piece_of(L, a0), p1 = piece_of(L, a1 - 1);
+                if (p0 != p1) S.job[atomicAdd(&S.n_job, 1)] = make_int4(r, row, p0, p1);   // else finished in place
+            }
+        }
+        __syncthreads();
+        const int n_job = S.n_job;
+        if (n_job > 0) grid_dep_wait();   // the decode kernel's partials
+        for (int ji = 0; ji < n_job; ++ji) {
+            const int4 job = S.job[ji];
+            float M = -INFINITY, L = 0.f;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int b = job.z; b <= job.w; b += kCombineStage) {
+                const int nb = min(kCombineStage, job.w - b + 1);
+                if (threadIdx.x == 0) {
+                    fence_proxy_async_smem();   // earlier reads of the stage before the copies' writes
+                    mbar_arrive_expect_tx(&S.full, (uint32_t)(nb * (kCombineAccBytes + kCombineMlBytes)));
+                    const uint64_t pol = policy_evict_first();
+                    for (int j = 0; j < nb; ++j) {
+                        const size_t slot = (size_t)job.x + b + j;
+                        bulk_load(S.acc[j], part_acc + (slot * kNumQHeads + half * kCombineHeads) * kHeadDim,
+                                  kCombineAccBytes, &S.full, pol);
+                        bulk_load(S.ml[j], part_ml + slot * kNumQHeads + half * kCombineHeads, kCombineMlBytes, &S.full,
+                                  pol);
+                    }
+                }
+                if (!mbar_wait(&S.full, phase)) {
+                    // the copies did not land within the wait limit; they target this CTA's shared
+                    // memory, so give them another bounded wait before leaving
+                    if (lane == 0) raise_error(err, kErrTimeout);
+                    if (threadIdx.x == 0) mbar_wait(&S.full, phase);
+                    return;
+                }
+                phase ^= 1;
+                for (int j = 0; j < nb; ++j) {
+                    const float2 ml = S.ml[j][warp];
+                    const float4 v = reinterpret_cast<const float4*>(S.acc[j][warp])[lane];
+                    const float Mn = fmaxf(M, ml.x);   // finite: every piece holds a key
+                    const float c = fast_exp2(M - Mn), w = fast_exp2(ml.x - Mn);
+                    L = fmaf(L, c, ml.y * w);
+                    o.x = fmaf(o.x, c, v.x * w);
+                    o.y = fmaf(o.y, c, v.y * w);
+                    o.z = fmaf(o.z, c, v.z * w);
+                    o.w = fmaf(o.w, c, v.w * w);
+                    M = Mn;
+                }
+                __syncthreads();   // the stage is free again
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            uint2 wv;
+            wv.x = pack_bf16x2(o.x * inv, o.y * inv);
+            wv.y = pack_bf16x2(o.z * inv, o.w * inv);
+            reinterpret_cast<uint2*>(out + (size_t)job.y * kQRowElems + head * kHeadDim)[lane] = wv;
+        }
+        __syncthreads();   // S.job and S.n_job are rewritten next round
+    }
+    grid_dep_launch();
 }
 
 // CTAs that run at once: one per SM, or fewer when the pool asks for fewer.
@@ -546,18 +807,47 @@ cudaError_t launch_decode(const StepArgs& a, const CUtensorMap* tmap_k, const CU
     const StepLayout& L = a.lay;
     const size_t smem = sizeof(DecodeSmem) + 1024;
     const int wave = decode_wave(a);
-    return launch_pdl(decode_kernel, dim3(decode_grid(a, wave)), dim3(kDecThreads), smem, stream, *tmap_k, *tmap_v,
-                      static_cast<const __nv_bfloat16*>(a.q), static_cast<__nv_bfloat16*>(a.out), a.cu_seqlens_q,
-                      a.context_lens, a.block_tables, a.max_blocks_per_seq, a.num_blocks,
-                      reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs, wave,
-                      reinterpret_cast<const int32_t*>(a.ws + L.counters_off),
-                      reinterpret_cast<float*>(a.ws + L.part_acc_off), reinterpret_cast<float2*>(a.ws + L.part_ml_off),
-                      reinterpret_cast<int32_t*>(a.ws + L.seg_count_off), a.softmax_scale * 1.4426950408889634f, a.err);
+    DecodeArgs d;
+    d.q = static_cast<const __nv_bfloat16*>(a.q);
+    d.out = static_cast<__nv_bfloat16*>(a.out);
+    d.cu = a.cu_seqlens_q;
+    d.ctx = a.context_lens;
+    d.tables = a.block_tables;
+    d.max_blocks = a.max_blocks_per_seq;
+    d.num_blocks = a.num_blocks;
+    d.page_off = reinterpret_cast<const int32_t*>(a.ws + L.page_off_off);
+    d.num_reqs = a.num_reqs;
+    d.wave = wave;
+    d.counters = reinterpret_cast<int32_t*>(a.ws + L.counters_off);
+    d.part_acc = reinterpret_cast<float*>(a.ws + L.part_acc_off);
+    d.part_ml = reinterpret_cast<float2*>(a.ws + L.part_ml_off);
+    d.scale_log2 = a.softmax_scale * 1.4426950408889634f;
+    d.err = a.err;
+    return launch_pdl(decode_kernel, dim3(decode_grid(a, wave)), dim3(kDecThreads), smem, stream, *tmap_k, *tmap_v, d);
+}
+
+cudaError_t launch_combine(const StepArgs& a, cudaStream_t stream) {
+    const StepLayout& L = a.lay;
+    const int wave = decode_wave(a);
+    // two CTAs per row; no more CTAs than run at once (two per SM), each pair then taking
+    // several rows
+    long long grid = 2LL * a.num_reqs;
+    const long long cap = 2LL * (a.num_sms > 0 ? a.num_sms : 1);
+    if (grid > cap) grid = cap;
+    if (grid < 2) grid = 2;
+    return launch_pdl(combine_kernel, dim3((unsigned)grid), dim3(kCombineThreads), sizeof(CombineSmem) + 128, stream,
+                      reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs, a.cu_seqlens_q,
+                      reinterpret_cast<const int32_t*>(a.ws + L.counters_off), wave, decode_grid(a, wave),
+                      reinterpret_cast<const float*>(a.ws + L.part_acc_off),
+                      reinterpret_cast<const float2*>(a.ws + L.part_ml_off), static_cast<__nv_bfloat16*>(a.out), a.err);
 }
 
 cudaError_t configure_decode_kernel() {
-    return cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)(sizeof(DecodeSmem) + 1024));
+    const cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)(sizeof(DecodeSmem) + 1024));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(sizeof(CombineSmem) + 128));
 }
 
 }  // namespace kvp

@@ -7,8 +7,8 @@
 //   q_r == 1 (decode): its history of ctx_r + 1 keys covers ceil((ctx_r+1)/16) blocks;
 //     page_off[r] is the exclusive prefix sum of those block counts over the requests
 //     (0 blocks for other requests), page_off[num_reqs] the total.  The decode kernel
-//     shares the total out evenly among its CTAs; seg_count[r] (zeroed here) counts the
-//     CTAs that finished their part of a split row.
+//     shares the total out among its CTAs; counters[4] (zeroed here) counts the chunks
+//     of their ranges' tails the decode CTAs have taken.
 //   q_r >= 2 (prefill chunk): one tile per 64 query tokens (two MMA tiles of 32 tokens x
 //     4 query heads of a KV group), emitted last tile first so the longest tiles start
 //     earliest.
@@ -75,7 +75,7 @@ __device__ __forceinline__ int2 warp_incl_scan(int2 v, int lane) {
 __global__ void __launch_bounds__(kPrepThreads) step_prep_kernel(
     const int32_t* __restrict__ cu, const int32_t* __restrict__ ctx, int num_reqs, int num_tokens, int max_q_len,
     int max_context_len, int max_blocks, int max_prefill_tiles, int num_sms, int32_t* __restrict__ counters,
-    int32_t* __restrict__ page_off, int32_t* __restrict__ seg_count, int4* __restrict__ pre_tiles,
+    int32_t* __restrict__ page_off, int4* __restrict__ pre_tiles,
     uint32_t* __restrict__ err) {
     __shared__ int s_ok;
     __shared__ int2 s_warp[32];
@@ -131,7 +131,6 @@ __global__ void __launch_bounds__(kPrepThreads) step_prep_kernel(
         const int dz = base.y + wex.y + incl.y - n.y;
         if (r < num_reqs) {
             page_off[r] = dx;
-            seg_count[r] = 0;
         }
         if (n.y > 0) {
             if (dz + n.y > max_prefill_tiles) {
@@ -159,6 +158,7 @@ __global__ void __launch_bounds__(kPrepThreads) step_prep_kernel(
         counters[1] = min(b.y, max_prefill_tiles);
         counters[2] = decode_sm_share(b.x, w * kNumKvHeads, num_sms);
         counters[3] = 0;
+        counters[4] = 0;
     }
     // This kernel reads nothing the previous one (kv_append) writes, so it ran alongside
     // it; it finishes only after that kernel has, so that later kernels, which wait for
@@ -179,8 +179,6 @@ StepLayout make_step_layout(int num_reqs, int num_tokens) {
     off = up(off + 8 * sizeof(int32_t));
     L.page_off_off = off;
     off = up(off + ((size_t)num_reqs + 1) * sizeof(int32_t));
-    L.seg_count_off = off;
-    off = up(off + (size_t)num_reqs * sizeof(int32_t));
     L.prefill_tiles_off = off;
     off = up(off + (size_t)L.max_prefill_tiles * sizeof(int4));
     L.part_acc_off = off;
@@ -198,7 +196,6 @@ cudaError_t launch_step_prep(const StepArgs& a, cudaStream_t stream) {
                       L.max_prefill_tiles, a.num_sms > 0 ? a.num_sms : 1,
                       reinterpret_cast<int32_t*>(a.ws + L.counters_off),
                       reinterpret_cast<int32_t*>(a.ws + L.page_off_off),
-                      reinterpret_cast<int32_t*>(a.ws + L.seg_count_off),
                       reinterpret_cast<int4*>(a.ws + L.prefill_tiles_off), a.err);
 }
 

@@ -508,6 +508,8 @@ kvp_status paged_attention_step(kvp_pool* p, const void* q, void* out, const int
                          [&] { return kvp::launch_prefill(a, &tq, &p->tmap_k, &p->tmap_v, s); }) != cudaSuccess)
             return KVP_E_CUDA;
     }
+    if (timed_launch(p, KVP_KERNEL_COMBINE, s, [&] { return kvp::launch_combine(a, s); }) != cudaSuccess)
+        return KVP_E_CUDA;
     return KVP_OK;
 }
 

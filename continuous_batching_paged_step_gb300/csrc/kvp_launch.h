@@ -16,10 +16,10 @@ namespace kvp {
 // Offsets are in bytes from the workspace base; every region is 256-byte aligned.
 struct StepLayout {
     int max_prefill_tiles;   // (request, 32-token q tile) work items of prefill chunks
-    int max_partials;        // split-KV partial slots: request r cut by CTA c uses r + c
-    size_t counters_off;     // int32[8]: 1 = prefill tiles, 2 = decode CTAs, 3 = prefill CTAs done
+    int max_partials;        // split-KV partial slots: request r cut by decode piece p uses r + p
+    size_t counters_off;     // int32[8]: 1 = prefill tiles, 2 = decode CTAs, 3 = prefill CTAs done,
+                             // 4 = decode chunks taken
     size_t page_off_off;     // int32 [num_reqs + 1]: first global decode block of each request
-    size_t seg_count_off;    // int32 [num_reqs]: CTAs done with their part of a split decode row
     size_t prefill_tiles_off;// int4 {r, first token of tile, tokens in tile, 0}
     size_t part_acc_off;     // float [slot][32 heads][128]  (unnormalised)
     size_t part_ml_off;      // float2 [slot][32 heads]      (running max (log2 units), sum)
@@ -61,6 +61,9 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t
 cudaError_t launch_step_prep(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const StepArgs& a, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
                           cudaStream_t stream);
+// Merge the split-KV partials of decode rows cut into several pieces (after the decode
+// kernel and, when there is one, the prefill kernel).
+cudaError_t launch_combine(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const StepArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
                            const CUtensorMap* tmap_v, cudaStream_t stream);
 

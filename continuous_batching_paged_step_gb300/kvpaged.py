@@ -49,7 +49,7 @@ SIGNATURES = {
     "kv_blocks_swap_out": (_I, [_P, _I, _I32P, _P, _P, _P]),
     "kv_blocks_swap_in": (_I, [_P, _I, _P, _P, _I32P, _P]),
 }
-KERNEL_NAMES = ("kv_append", "step_prep", "prefill_tcgen05", "decode_splitkv", "block_move")
+KERNEL_NAMES = ("kv_append", "step_prep", "prefill_tcgen05", "decode_splitkv", "block_move", "splitkv_combine")
 BLOCK_BYTES = N_KV_HEADS * BLOCK_SIZE * HEAD_DIM * 2   # one block of K (or of V): 32 KiB
 
 

@@ -217,7 +217,8 @@ KVP_API size_t paged_attention_workspace_size(const kvp_pool* pool, int num_reqs
  * Rows with q_len == 1 (decode) take the HBM-bound split-KV path; rows of requests with
  * q_len > 1 (prefill chunks) take the tcgen05 tensor-core path.  The two kernels run side
  * by side on disjoint SMs (the step's first kernel sizes the decode's share from the
- * step's work); the call's work is complete, in stream order, when both are. */
+ * step's work); a last kernel merges the partial results of decode rows that the split
+ * cut into pieces.  The call's work is complete, in stream order, when that kernel is. */
 KVP_API kvp_status paged_attention_step(kvp_pool* pool, const void* q, void* out,
                                 const int32_t* cu_seqlens_q, const int32_t* context_lens,
                                 const int32_t* block_tables, int max_blocks_per_seq,
@@ -228,11 +229,14 @@ KVP_API kvp_status paged_attention_step(kvp_pool* pool, const void* q, void* out
 /* Decode split: the 16-token blocks of all decode rows of a step are shared out evenly,
  * in request order, among `ctas` CTAs at a time (0 = one per SM, the default; at most
  * 1024; a step that also has prefill chunks gives the decode at most the share of SMs its
- * metadata kernel leaves it); a CTA takes at most 2,048 blocks, so a step with more than ctas x 2,048 decode
- * blocks runs in several waves of CTAs (at most 1024 CTAs in all: a step whose decode rows
- * hold more blocks than that allows sets KVP_ERRBIT_BAD_META).  A row whose blocks fall to
- * several CTAs is finished by a merge of their partial results.  The workspace size does
- * not depend on this setting.  Host-only. */
+ * metadata kernel leaves it); a CTA's range holds at most 1,024 blocks, so a step with
+ * more than ctas x 1,024 decode blocks runs in several waves of CTAs (at most 1024 CTAs in
+ * all: a step whose decode rows hold more blocks than that allows sets
+ * KVP_ERRBIT_BAD_META).  The last fifth of each range is handed out in small chunks to
+ * whichever CTA runs out of work first, so that SMs that stream more slowly finish with
+ * the others.  A row whose blocks fall to several pieces (ranges or chunks) is finished by
+ * a merge of their partial results.  The workspace size does not depend on this setting.
+ * Host-only. */
 KVP_API kvp_status kv_pool_set_decode_ctas(kvp_pool* pool, int ctas);
 
 /* Synchronise `stream`, then read and clear the pool's device error word.  *bits (may be
@@ -278,9 +282,10 @@ KVP_API size_t paged_attention_noalloc_capacity(void);
 #define KVP_KERNEL_APPEND  0
 #define KVP_KERNEL_PREP    1
 #define KVP_KERNEL_PREFILL 2
-#define KVP_KERNEL_DECODE  3   /* split-KV partials are merged inside this kernel */
+#define KVP_KERNEL_DECODE  3   /* split-KV partials of decode rows cut into several pieces */
 #define KVP_KERNEL_BLOCKS  4   /* block copies of kv_block_cow / kv_blocks_swap_* */
-#define KVP_NUM_KERNELS    5
+#define KVP_KERNEL_COMBINE 5   /* merges those partials */
+#define KVP_NUM_KERNELS    6
 KVP_API kvp_status kv_pool_enable_timing(kvp_pool* pool, int max_launches);
 KVP_API kvp_status kv_pool_read_timing(kvp_pool* pool, int* counts, float* ms);
 

@@ -94,10 +94,11 @@ def test_decode_split_and_combine(runner, ctas):
 
 @pytest.mark.parametrize("ctas", [1, 2])
 def test_decode_ranges_beyond_staged_ids(runner, ctas):
-    # 2,504 decode blocks: with one CTA at a time no range fits the 2,048 block ids a CTA
-    # stages, so the blocks are shared out over two waves of one CTA (rows split across
-    # waves are merged by the later CTA); with two CTAs at a time one wave suffices.  A
-    # prefill chunk rides along, so the metadata kernel's SM split is exercised too.
+    # 2,504 decode blocks: with one CTA at a time no range fits the 1,024 blocks a CTA's
+    # range may hold, so the blocks are shared out over three waves of one CTA (chunks of
+    # a range's tail go to whichever CTA asks first, in any wave); with two CTAs at a time
+    # over two waves.  Rows split across CTAs are merged by the combine kernel.  A prefill
+    # chunk rides along, so the metadata kernel's SM split is exercised too.
     spec = wl.StepSpec("long-decode", q_lens=[1, 1, 1, 1, 1, 70], ctx_lens=[8000, 7990, 8016, 7999, 8001, 100],
                        num_blocks=2700, seed=515)
     _run_full_check(runner, spec, ctas=ctas)
