@@ -178,10 +178,20 @@ __device__ __forceinline__ Layout make_layout(int P, int G) {
     return L;
 }
 
-// Tail of a range of n blocks: >= pp - 1 when pp > 1, so that no chunk is empty, and at
-// most kMaxChunk blocks per chunk.
+// Tail of a range of n blocks (0 when pp == 1).  Its n_ch = pp - 1 chunks shrink
+// linearly: chunk k (0-based) gets a share n_ch - k of n_ch (n_ch + 1) / 2, so the last
+// chunks handed out are the smallest and the CTAs that take them finish close together.
+// The tail holds at least n_ch (n_ch + 1) / 2 blocks (so that no chunk is empty: make_layout
+// keeps 4 n_ch <= n / 5 and n_ch <= 7) and at most 16 pp (so that the first, largest chunk
+// has at most 2 tail / pp <= kMaxChunk blocks).
 __device__ __forceinline__ int tail_blocks(const Layout& L, int n) {
-    return L.pp > 1 ? min(n * kTailPercent / 100, (L.pp - 1) * kMaxChunk) : 0;
+    return L.pp > 1 ? min(n * kTailPercent / 100, 16 * L.pp) : 0;
+}
+
+// First block of chunk k of a tail, relative to the tail's start (k = n_ch: the tail's size).
+__device__ __forceinline__ int chunk_start(int tail, int n_ch, int k) {
+    const int sk = k * n_ch - k * (k - 1) / 2, total = n_ch * (n_ch + 1) / 2;
+    return tail * sk / total;
 }
 
 // Global blocks [s, e) of piece pi.
@@ -196,8 +206,8 @@ __device__ __forceinline__ void piece_bounds(const Layout& L, int pi, int& s, in
         return;
     }
     const int n_ch = L.pp - 1;
-    s = mid + (int)((long long)tail * (j - 1) / n_ch);
-    e = mid + (int)((long long)tail * j / n_ch);
+    s = mid + chunk_start(tail, n_ch, j - 1);
+    e = mid + chunk_start(tail, n_ch, j);
 }
 
 // The piece holding global block x.
@@ -208,7 +218,9 @@ __device__ __forceinline__ int piece_of(const Layout& L, int x) {
     const int tail = tail_blocks(L, hi - lo), mid = hi - tail;
     if (x < mid) return c * L.pp;
     const int n_ch = L.pp - 1;
-    return c * L.pp + 1 + (int)(((long long)(x - mid + 1) * n_ch - 1) / tail);
+    int k = 0;
+    while (k + 1 < n_ch && chunk_start(tail, n_ch, k + 1) <= x - mid) ++k;
+    return c * L.pp + 1 + k;
 }
 
 // The largest r in [r_lo, num_reqs) with page_off[r] <= x (page_off[r_lo] <= x): the
