@@ -67,7 +67,8 @@ constexpr int kTailPercent = 20;   // share of each range handed out as chunks
 constexpr int kChunkTarget = 4;    // blocks per chunk, at least
 constexpr int kMaxPieces = 8;      // pieces per range: own part + chunks
 constexpr int kMaxChunk = 32;      // blocks per chunk, at most (one scheduler lane each)
-constexpr int kClaimLead = 8;      // blocks of the own part still to issue when the first chunk is claimed
+constexpr int kClaimLead = 3;      // blocks still to issue (own part or chunk) when the next chunk is claimed
+constexpr int kPageOffCap = 2047;  // requests whose block offsets a CTA stages in shared memory
 
 // segment flags next to a block's position in its request
 constexpr uint32_t kPosMask = 0x00FFFFFFu;
@@ -91,13 +92,15 @@ struct __align__(1024) DecodeSmem {
     BlockInfo meta[kDecStages];                 // block in each stage
     int piece[kDecStages];
     int chunk_n[2], chunk_piece[2];             // blocks (0: the pool is empty) and piece of each chunk buffer
-    int first_req, last_req;
+    int32_t page_off[kPageOffCap + 1];           // the step's block offsets, when they fit
     int stop;                                   // the producer asks the scheduler to leave
     uint64_t policy;
     uint64_t full[kDecStages], empty[kDecStages];
     uint64_t req;                               // producer -> scheduler: claim the next chunk
     uint64_t rdy[2];                            // scheduler -> producer: chunk buffer filled
 };
+
+static_assert(sizeof(DecodeSmem) + 1024 <= 227 * 1024, "decode CTA shared memory exceeds the per-CTA limit");
 
 // Tensor-map load with an L2 eviction hint.
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* tmap, int c0, int c1, uint32_t bar,
@@ -373,7 +376,18 @@ __device__ __forceinline__ void produce(DecodeSmem& S, const DecodeArgs& a, cons
     const bool pool = L.pp > 1;
     const int own_piece = (int)blockIdx.x * L.pp;
     const int claim_at = max(0, n_own - kClaimLead);
-    for (int q = 0; q < n_own && ok; ++q) {
+    // The first blocks (described by this warp) go out before the rest of the own part is
+    // described by the other warps; then the CTA meets once.
+    const int q_pre = min(kDecStages, n_own);
+    int q = 0;
+    for (; q < q_pre && ok; ++q) {
+        if (q == claim_at && pool) request();
+        if (lane == 0) ok = issue(S.own[q], own_piece);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        ++k;
+    }
+    __syncthreads();   // the own part is described; every warp sees the barriers initialised
+    for (; q < n_own && ok; ++q) {
         if (q == claim_at && pool) request();
         if (lane == 0) ok = issue(S.own[q], own_piece);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -383,9 +397,12 @@ __device__ __forceinline__ void produce(DecodeSmem& S, const DecodeArgs& a, cons
     bool sched_done = !pool;   // the scheduler has handed over an empty chunk and left
     if (ok && pool) n = receive(buf, piece);
     while (ok && n > 0) {
-        request();   // the chunk after this one, into the other buffer
-        for (int q = 0; q < n && ok; ++q) {
-            if (lane == 0) ok = issue(S.chunk[buf][q], piece);
+        // the chunk after this one (into the other buffer) is claimed kClaimLead blocks
+        // before this one is all issued
+        const int req_at = max(0, n - kClaimLead);
+        for (int j = 0; j < n && ok; ++j) {
+            if (j == req_at) request();
+            if (lane == 0) ok = issue(S.chunk[buf][j], piece);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             ++k;
         }
@@ -607,11 +624,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
     grid_dep_wait();     // block offsets, cache contents
     grid_dep_launch();
-    const int P = a.page_off[a.num_reqs];
+    // the block offsets go to shared memory (one coalesced pass) when they fit, so that
+    // every search below runs there
+    DecodeArgs b = a;
+    const int want = a.counters[2];   // the decode's share of the SMs (loaded alongside the offsets)
+    if (a.num_reqs <= kPageOffCap) {
+        for (int k = threadIdx.x; k <= a.num_reqs; k += kDecThreads) S.page_off[k] = a.page_off[k];
+        __syncthreads();
+        b.page_off = S.page_off;
+    }
+    const int32_t* po = b.page_off;
+    const int P = po[a.num_reqs];
     if (P <= 0) return;
     // SMs left to this step's prefill tiles run them meanwhile (unless the launch is too
     // small for the narrower waves that would need)
-    int G = decode_ctas_used(P, max(1, min(a.wave, a.counters[2])), gridDim.x);
+    int G = decode_ctas_used(P, max(1, min(a.wave, want)), gridDim.x);
     if (G == 0) G = decode_ctas_used(P, a.wave, gridDim.x);
     if (G == 0) {
         // the launch has too few CTAs for this many blocks (the host sizes it from an
@@ -629,66 +656,70 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         return;
     }
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kDecStages; ++s) {
-            mbar_init(&S.full[s], 1);
-            mbar_init(&S.empty[s], kConsumerWarps);
+    // ids, requests and positions of every block of the own part (requests found by
+    // searches between those of its first and its last block): the producer warp describes
+    // the first 32 and starts copying at once, the other warps describe the rest
+    const int r_first = request_of(po, a.num_reqs, 0, lo);
+    const int r_last = request_of(po, a.num_reqs, r_first, mid - 1);
+    auto describe = [&](int x) {
+        int ra = r_first, rb = r_last;   // largest r with page_off[r] <= x
+        while (ra < rb) {
+            const int m = (ra + rb + 1) >> 1;
+            if (po[m] <= x) ra = m;
+            else rb = m - 1;
         }
-        mbar_init(&S.req, 1);
-        mbar_init(&S.rdy[0], 1);
-        mbar_init(&S.rdy[1], 1);
-        S.stop = 0;
-        S.policy = policy_evict_first();
-        fence_barrier_init();
-    }
-    // requests holding the first and the last block of the own part (one parallel pass)
-    for (int r = threadIdx.x; r < a.num_reqs; r += kDecThreads) {
-        const int a0 = a.page_off[r], a1 = a.page_off[r + 1];
-        if (a0 <= lo && lo < a1) S.first_req = r;
-        if (a0 <= mid - 1 && mid - 1 < a1) S.last_req = r;
-    }
-    __syncthreads();
-    // ids, requests and positions of every block of the own part
-    {
-        const int r_first = S.first_req, r_last = S.last_req;
-        for (int x = lo + threadIdx.x; x < mid; x += kDecThreads) {
-            int ra = r_first, rb = r_last;   // largest r with page_off[r] <= x
-            while (ra < rb) {
-                const int m = (ra + rb + 1) >> 1;
-                if (a.page_off[m] <= x) ra = m;
-                else rb = m - 1;
+        S.own[x - lo] = block_info(x, ra, lo, mid, po, a.tables, a.max_blocks, a.num_blocks, a.cu, a.ctx, a.err);
+    };
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            for (int s = 0; s < kDecStages; ++s) {
+                mbar_init(&S.full[s], 1);
+                mbar_init(&S.empty[s], kConsumerWarps);
             }
-            S.own[x - lo] = block_info(x, ra, lo, mid, a.page_off, a.tables, a.max_blocks, a.num_blocks, a.cu, a.ctx,
-                                       a.err);
+            mbar_init(&S.req, 1);
+            mbar_init(&S.rdy[0], 1);
+            mbar_init(&S.rdy[1], 1);
+            S.stop = 0;
+            S.policy = policy_evict_first();
+            fence_barrier_init();
         }
+        if (lo + lane < mid) describe(lo + lane);
+        __syncwarp();
+        produce(S, b, &tmap_k, &tmap_v, L, n_own, lane);   // meets the other warps' __syncthreads
+        return;
     }
+    const int t = warp < kProducerWarp ? (int)threadIdx.x : (int)threadIdx.x - 32;   // among the other warps
+    for (int x = lo + 32 + t; x < mid; x += kDecThreads - 32) describe(x);
     __syncthreads();
-    if (warp == kProducerWarp) produce(S, a, &tmap_k, &tmap_v, L, n_own, lane);
-    else if (warp == kSchedulerWarp) {
-        if (L.pp > 1) schedule(S, a, L, lane);
-    } else consume(S, a, L, warp, lane);
+    if (warp == kSchedulerWarp) {
+        if (L.pp > 1) schedule(S, b, L, lane);
+    } else consume(S, b, L, warp, lane);
 }
 
 constexpr int kCombineHeads = kNumQHeads / 2;         // query heads of one combine CTA (half a row)
 constexpr int kCombineThreads = kCombineHeads * 32;   // one warp per query head
-constexpr int kCombineStage = 12;                     // pieces staged in shared memory at once
+constexpr int kCombineStageMax = 12;                  // pieces staged in shared memory at once (at most)
 constexpr int kCombineAccBytes = kCombineHeads * kHeadDim * 4;   // one piece's accumulators: 8 KiB
 constexpr int kCombineMlBytes = kCombineHeads * 8;               // one piece's (m, l): 128 B
 
 constexpr int kCombineRowsPerRound = 32;   // rows a CTA plans at once
 
+// Shared memory of a combine CTA staging `stage` pieces: this header, then the pieces'
+// accumulators (8 KiB each) and their (m, l) (128 B each).
 struct CombineSmem {
-    float acc[kCombineStage][kCombineHeads][kHeadDim];
-    float2 ml[kCombineStage][kCombineHeads];
     int4 job[kCombineRowsPerRound];   // {request, row, first piece, last piece} of the rows to merge
     int n_job;
     uint64_t full;
 };
 
+__host__ __device__ constexpr size_t combine_smem_bytes(int stage) {
+    return ((sizeof(CombineSmem) + 127) & ~size_t(127)) + (size_t)stage * (kCombineAccBytes + kCombineMlBytes) + 128;
+}
+
 // Split-KV combine: every decode row whose blocks the decode kernel cut into several
 // pieces gets O = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p over its pieces
 // (M = max_p m_p), merged online piece by piece.  Two CTAs per row (16 query heads each,
-// one warp per head, lane l holding dims 4l .. 4l + 3); a CTA stages up to kCombineStage
+// one warp per head, lane l holding dims 4l .. 4l + 3); a CTA stages up to `stage`
 // pieces' partials at once in shared memory with bulk copies, so a row costs about one
 // round trip to memory.  Rows held by one piece were finished in place.  Launched after
 // the step's attention kernels, as a programmatic dependent: before its wait it works out
@@ -703,9 +734,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const int32_t*
                                                                    const float* __restrict__ part_acc,
                                                                    const float2* __restrict__ part_ml,
                                                                    __nv_bfloat16* __restrict__ out,
-                                                                   uint32_t* __restrict__ err) {
+                                                                   uint32_t* __restrict__ err, int stage) {
     extern __shared__ uint8_t smem_raw[];
-    CombineSmem& S = *reinterpret_cast<CombineSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    CombineSmem& S = *reinterpret_cast<CombineSmem*>(base);
+    float* s_acc = reinterpret_cast<float*>(base + ((sizeof(CombineSmem) + 127) & ~size_t(127)));   // [stage][16][128]
+    float2* s_ml = reinterpret_cast<float2*>(s_acc + (size_t)stage * kCombineHeads * kHeadDim);      // [stage][16]
     const int half = blockIdx.x & 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int head = half * kCombineHeads + warp;
@@ -743,17 +777,19 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const int32_t*
             const int4 job = S.job[ji];
             float M = -INFINITY, L = 0.f;
             float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int b = job.z; b <= job.w; b += kCombineStage) {
-                const int nb = min(kCombineStage, job.w - b + 1);
+            for (int b = job.z; b <= job.w; b += stage) {
+                const int nb = min(stage, job.w - b + 1);
                 if (threadIdx.x == 0) {
                     fence_proxy_async_smem();   // earlier reads of the stage before the copies' writes
                     mbar_arrive_expect_tx(&S.full, (uint32_t)(nb * (kCombineAccBytes + kCombineMlBytes)));
                     const uint64_t pol = policy_evict_first();
                     for (int j = 0; j < nb; ++j) {
                         const size_t slot = (size_t)job.x + b + j;
-                        bulk_load(S.acc[j], part_acc + (slot * kNumQHeads + half * kCombineHeads) * kHeadDim,
-                                  kCombineAccBytes, &S.full, pol);
-                        bulk_load(S.ml[j], part_ml + slot * kNumQHeads + half * kCombineHeads, kCombineMlBytes, &S.full,
+                        bulk_load(s_acc + (size_t)j * kCombineHeads * kHeadDim,
+                                  part_acc + (slot * kNumQHeads + half * kCombineHeads) * kHeadDim, kCombineAccBytes,
+                                  &S.full, pol);
+                        bulk_load(s_ml + j * kCombineHeads, part_ml + slot * kNumQHeads + half * kCombineHeads,
+                                  kCombineMlBytes, &S.full,
                                   pol);
                     }
                 }
@@ -766,8 +802,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const int32_t*
                 }
                 phase ^= 1;
                 for (int j = 0; j < nb; ++j) {
-                    const float2 ml = S.ml[j][warp];
-                    const float4 v = reinterpret_cast<const float4*>(S.acc[j][warp])[lane];
+                    const float2 ml = s_ml[j * kCombineHeads + warp];
+                    const float4 v = reinterpret_cast<const float4*>(s_acc + ((size_t)j * kCombineHeads + warp) * kHeadDim)[lane];
                     const float Mn = fmaxf(M, ml.x);   // finite: every piece holds a key
                     const float c = fast_exp2(M - Mn), w = fast_exp2(ml.x - Mn);
                     L = fmaf(L, c, ml.y * w);
@@ -841,17 +877,20 @@ cudaError_t launch_decode(const StepArgs& a, const CUtensorMap* tmap_k, const CU
 cudaError_t launch_combine(const StepArgs& a, cudaStream_t stream) {
     const StepLayout& L = a.lay;
     const int wave = decode_wave(a);
-    // two CTAs per row; no more CTAs than run at once (two per SM), each pair then taking
-    // several rows
+    // Two CTAs per row, and no more CTAs than run at once (two per SM, each staging up to
+    // 12 pieces), each pair then taking several rows.  (Three CTAs per SM staging 8 pieces
+    // each merged the 256-row decode step more slowly: its longest rows took more rounds.)
+    const int stage = kCombineStageMax;
     long long grid = 2LL * a.num_reqs;
     const long long cap = 2LL * (a.num_sms > 0 ? a.num_sms : 1);
     if (grid > cap) grid = cap;
     if (grid < 2) grid = 2;
-    return launch_pdl(combine_kernel, dim3((unsigned)grid), dim3(kCombineThreads), sizeof(CombineSmem) + 128, stream,
+    return launch_pdl(combine_kernel, dim3((unsigned)grid), dim3(kCombineThreads), combine_smem_bytes(stage), stream,
                       reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs, a.cu_seqlens_q,
                       reinterpret_cast<const int32_t*>(a.ws + L.counters_off), wave, decode_grid(a, wave),
                       reinterpret_cast<const float*>(a.ws + L.part_acc_off),
-                      reinterpret_cast<const float2*>(a.ws + L.part_ml_off), static_cast<__nv_bfloat16*>(a.out), a.err);
+                      reinterpret_cast<const float2*>(a.ws + L.part_ml_off), static_cast<__nv_bfloat16*>(a.out), a.err,
+                      stage);
 }
 
 cudaError_t configure_decode_kernel() {
@@ -859,7 +898,7 @@ cudaError_t configure_decode_kernel() {
                                                (int)(sizeof(DecodeSmem) + 1024));
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)(sizeof(CombineSmem) + 128));
+                                (int)combine_smem_bytes(kCombineStageMax));
 }
 
 }  // namespace kvp

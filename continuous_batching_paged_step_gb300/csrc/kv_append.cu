@@ -33,6 +33,21 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
     __shared__ int32_t s_cu[kAppendSmemReqs + 1];
     __shared__ int32_t s_ctx[kAppendSmemReqs];
     grid_dep_launch();   // the step's metadata kernel does not read the pool
+    const int lane = threadIdx.x & 31;
+    const int i = blockIdx.x * kAppendRowsPerCta + (threadIdx.x >> 5);
+    // The row's K and V first: their loads do not depend on where the row goes, so they
+    // are in flight while the metadata below is looked up.
+    constexpr int kRowChunks = kKvRowElems * 2 / 16;   // 128 chunks of 16 bytes per row and tensor
+    constexpr int kLaneChunks = kRowChunks / 32;
+    const size_t src = (size_t)i * kRowChunks;
+    uint4 kv[kLaneChunks], vv[kLaneChunks];
+    if (i < num_tokens) {
+#pragma unroll
+        for (int k = 0; k < kLaneChunks; ++k) {
+            kv[k] = k_new[src + k * 32 + lane];
+            vv[k] = v_new[src + k * 32 + lane];
+        }
+    }
     const bool staged = num_reqs <= kAppendSmemReqs;
     if (staged) {
         for (int k = threadIdx.x; k <= num_reqs; k += blockDim.x) s_cu[k] = cu[k];
@@ -41,8 +56,6 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
     }
     const int32_t* cu_r = staged ? s_cu : cu;
     const int32_t* ctx_r = staged ? s_ctx : ctx;
-    const int lane = threadIdx.x & 31;
-    const int i = blockIdx.x * kAppendRowsPerCta + (threadIdx.x >> 5);
     if (i >= num_tokens) return;
     long long dst = -1;   // element-chunk index of (block, head 0, slot), or -1
     if (lane == 0) {
@@ -79,18 +92,14 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
     }
     dst = __shfl_sync(0xffffffffu, dst, 0);
     if (dst < 0) return;
-    constexpr int kRowChunks = kKvRowElems * 2 / 16;   // 128 chunks of 16 bytes per row and tensor
-    const size_t src = (size_t)i * kRowChunks;
 #pragma unroll
-    for (int k = 0; k < kRowChunks / 32; ++k) {
+    for (int k = 0; k < kLaneChunks; ++k) {
         const int j = k * 32 + lane;
         const int h = j >> 4, chunk = j & 15;
         // (block, head h, slot) tile offset: head stride is 16 slots of 256 bytes
         const size_t d = (size_t)dst + (size_t)h * kBlockSize * (kHeadBytes / 16) + chunk;
-        const uint4 kv = k_new[src + j];
-        const uint4 vv = v_new[src + j];
-        k_cache[d] = kv;
-        v_cache[d] = vv;
+        k_cache[d] = kv[k];
+        v_cache[d] = vv[k];
     }
 }
 
