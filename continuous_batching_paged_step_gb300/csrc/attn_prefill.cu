@@ -80,6 +80,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+// True in exactly one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(p));
+    return p != 0;
+}
+
 // Softmax and epilogue of one MMA tile (a warpgroup, one thread per row).
 __device__ __forceinline__ void softmax_tile(PrefillSmem& S, const PrefillArgs& a, uint32_t tmem, int t, int wq,
                                              int lane, int g, int row0, int qpos0, int ntok_t, int nt, int n_kt,
@@ -320,35 +331,36 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tmap_q, const CUt
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------------------ MMA issuer
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, 1);
-            // Descriptors are built once: Q tiles, K stages and V stages are 32 KiB apart
-            // and a K step moves 32 bytes inside the swizzle rows (or to the next 64-dim
-            // half), so every MMA's operands are a constant step from these bases (the
-            // 14-bit address field never carries: shared addresses stay below 227 KiB).
-            // With a descriptor rebuilt per MMA, this one thread, not the tensor core,
-            // set the pace.
-            constexpr uint64_t kStep32K = (2 * kHalfBytes) >> 4;
-            const uint64_t q_desc0 = smem_desc_sw128(smem_u32(S.q[0][0]), 16, 1024);
-            const uint64_t k_desc0 = smem_desc_sw128(smem_u32(S.k[0][0]), 16, 1024);
-            const uint64_t v_desc0 = smem_desc_sw128(smem_u32(S.v[0][0]), kHalfBytes, 1024);
-            bool ok = mbar_wait(&S.q_full, 0);
-            // Waits and issues are kept apart: each round first waits for everything it
-            // needs (the next K tile, which is normally long there, then this tile's P and
-            // V), then issues P.V and the next Q K^T back to back, so that the tensor core
-            // has 16 MMAs queued while the thread waits for the other tile.
-            auto wait_k = [&](int kt) -> bool {
-                return mbar_wait(&S.k_full[kt % kKStages], (kt / kKStages) & 1);
-            };
-            auto wait_pv = [&](int t, int kt) -> bool {
-                return mbar_wait(&S.p_full[t], kt & 1) && mbar_wait(&S.v_full[kt % kVStages], (kt / kVStages) & 1);
-            };
-            auto mma_qk = [&](int t, int kt) {
-                const int s = kt % kKStages;
-                const uint64_t qa = q_desc0 + (uint64_t)t * kStep32K, kb = k_desc0 + (uint64_t)s * kStep32K;
-                const uint32_t d = tmem + t * 128;
+        // ---------------------------------------------------------------- MMA issuer
+        // The whole warp runs the loop in step (waits, descriptor arithmetic: values the
+        // same in every lane), and one elected lane issues each tcgen05 instruction.  With
+        // the loop on lane 0 alone, that thread took ~80 cycles per MMA, more than the
+        // tensor core's 64.
+        const bool leader = elect_one();
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, 1);
+        // Descriptors are built once: Q tiles, K stages and V stages are 32 KiB apart
+        // and a K step moves 32 bytes inside the swizzle rows (or to the next 64-dim
+        // half), so every MMA's operands are a constant step from these bases (the
+        // 14-bit address field never carries: shared addresses stay below 227 KiB).
+        constexpr uint64_t kStep32K = (2 * kHalfBytes) >> 4;
+        const uint64_t q_desc0 = smem_desc_sw128(smem_u32(S.q[0][0]), 16, 1024);
+        const uint64_t k_desc0 = smem_desc_sw128(smem_u32(S.k[0][0]), 16, 1024);
+        const uint64_t v_desc0 = smem_desc_sw128(smem_u32(S.v[0][0]), kHalfBytes, 1024);
+        bool ok = warp_wait(&S.q_full, 0);
+        // Waits and issues are kept apart: each round first waits for everything it
+        // needs (the next K tile, which is normally long there, then this tile's P and
+        // V), then issues P.V and the next Q K^T back to back, so that the tensor core
+        // has 16 MMAs queued while the warp waits for the other tile.
+        auto wait_k = [&](int kt) -> bool { return warp_wait(&S.k_full[kt % kKStages], (kt / kKStages) & 1); };
+        auto wait_pv = [&](int t, int kt) -> bool {
+            return warp_wait(&S.p_full[t], kt & 1) && warp_wait(&S.v_full[kt % kVStages], (kt / kVStages) & 1);
+        };
+        auto mma_qk = [&](int t, int kt) {
+            const int s = kt % kKStages;
+            const uint64_t qa = q_desc0 + (uint64_t)t * kStep32K, kb = k_desc0 + (uint64_t)s * kStep32K;
+            const uint32_t d = tmem + t * 128;
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t koff = (uint64_t)((((kk >> 2) * kHalfBytes) + (kk & 3) * 32) >> 4);
@@ -356,44 +368,52 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tmap_q, const CUt
                 }
                 tc_commit(&S.s_full[t]);
                 if (t == 1 || kt >= nB) tc_commit(&S.k_empty[s]);   // last QK that reads this K stage
-            };
-            auto mma_pv = [&](int t, int kt) {
-                const int s = kt % kVStages;
-                const uint64_t vb = v_desc0 + (uint64_t)s * kStep32K;
-                const uint32_t d = tmem + 256 + t * 128, pa = tmem + t * 128;
-                const uint32_t acc0 = kt > 0 ? 1u : 0u;
+            }
+            __syncwarp();
+        };
+        auto mma_pv = [&](int t, int kt) {
+            const int s = kt % kVStages;
+            const uint64_t vb = v_desc0 + (uint64_t)s * kStep32K;
+            const uint32_t d = tmem + 256 + t * 128, pa = tmem + t * 128;
+            const uint32_t acc0 = kt > 0 ? 1u : 0u;
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     tc_mma_f16_ts(d, pa + kk * 8, vb + (uint64_t)((kk * 2048) >> 4), idesc_pv, kk > 0 ? 1u : acc0);
                 if (t == 1 || kt >= nB) tc_commit(&S.v_empty[s]);   // last P V that reads this V stage
-            };
-            if (ok && n_kt > 0 && (ok = wait_k(0))) {
-                tc_fence_after();
-                if (nA > 0) mma_qk(0, 0);
-                if (nB > 0) mma_qk(1, 0);
             }
-            for (int kt = 0; kt < n_kt && ok; ++kt) {
-                const bool more = kt + 1 < n_kt;   // the next K tile is needed by some MMA tile
-                if (kt < nA) {
-                    if (!(ok = (!more || wait_k(kt + 1)) && wait_pv(0, kt))) break;
-                    tc_fence_after();
-                    mma_pv(0, kt);
-                    if (kt + 1 < nA) mma_qk(0, kt + 1);
-                    else tc_commit(&S.o_done[0]);
-                }
-                if (kt < nB) {
-                    if (!(ok = (!more || wait_k(kt + 1)) && wait_pv(1, kt))) break;
-                    tc_fence_after();
-                    mma_pv(1, kt);
-                    if (kt + 1 < nB) mma_qk(1, kt + 1);
-                    else tc_commit(&S.o_done[1]);
-                }
-            }
-            if (!ok) raise_error(a.err, kErrTimeout);
-            // No MMA may still be running when TMEM is released.
-            tc_commit(&S.mma_done);
-            if (!mbar_wait(&S.mma_done, 0)) raise_error(a.err, kErrTimeout);
+            __syncwarp();
+        };
+        auto commit = [&](uint64_t* bar) {
+            if (leader) tc_commit(bar);
+            __syncwarp();
+        };
+        if (ok && n_kt > 0 && (ok = wait_k(0))) {
+            tc_fence_after();
+            if (nA > 0) mma_qk(0, 0);
+            if (nB > 0) mma_qk(1, 0);
         }
+        for (int kt = 0; kt < n_kt && ok; ++kt) {
+            const bool more = kt + 1 < n_kt;   // the next K tile is needed by some MMA tile
+            if (kt < nA) {
+                if (!(ok = (!more || wait_k(kt + 1)) && wait_pv(0, kt))) break;
+                tc_fence_after();
+                mma_pv(0, kt);
+                if (kt + 1 < nA) mma_qk(0, kt + 1);
+                else commit(&S.o_done[0]);
+            }
+            if (kt < nB) {
+                if (!(ok = (!more || wait_k(kt + 1)) && wait_pv(1, kt))) break;
+                tc_fence_after();
+                mma_pv(1, kt);
+                if (kt + 1 < nB) mma_qk(1, kt + 1);
+                else commit(&S.o_done[1]);
+            }
+        }
+        if (!ok && leader) raise_error(a.err, kErrTimeout);
+        // No MMA may still be running when TMEM is released.
+        commit(&S.mma_done);
+        if (!warp_wait(&S.mma_done, 0) && leader) raise_error(a.err, kErrTimeout);
     } else if (warp >= 4) {
         // --------------------------------------------------------- softmax + epilogue
         const int t = (warp - 4) >> 2;
