@@ -342,20 +342,26 @@ __device__ __forceinline__ void produce(DecodeSmem& S, const DecodeArgs& a, cons
                                         const CUtensorMap* tv, const Layout& L, int n_own, int lane) {
     int k = 0;   // blocks issued
     bool ok = true;
-    // lane 0: wait for stage k % kDecStages to be free, describe the block, copy it
+    // Whole warp, in step: wait for stage k % kDecStages to be free; one elected lane
+    // describes the block and issues its copies (operands the same in every lane: a lone
+    // lane running this loop issued its instructions far more slowly).
+    const bool leader = elect_one();
     auto issue = [&](const BlockInfo& b, int piece) -> bool {
         const int st = k % kDecStages;
-        if (!mbar_wait(&S.empty[st], ((k / kDecStages) & 1) ^ 1)) return false;
-        S.meta[st] = b;
-        S.piece[st] = piece;
+        if (!warp_wait(&S.empty[st], ((k / kDecStages) & 1) ^ 1)) return false;
         const int y = b.id * kBlockRows;
         const uint32_t bar = smem_u32(&S.full[st]);
         const uint32_t d = smem_u32(S.kv[st][0][0]);
-        mbar_arrive_expect_tx(&S.full[st], kStageBytes);
-        tma_load_2d_hint(d, tk, 0, y, bar, S.policy);
-        tma_load_2d_hint(d + kHalfTile, tk, 64, y, bar, S.policy);
-        tma_load_2d_hint(d + 2 * kHalfTile, tv, 0, y, bar, S.policy);
-        tma_load_2d_hint(d + 3 * kHalfTile, tv, 64, y, bar, S.policy);
+        if (leader) {
+            S.meta[st] = b;
+            S.piece[st] = piece;
+            mbar_arrive_expect_tx(&S.full[st], kStageBytes);
+            tma_load_2d_hint(d, tk, 0, y, bar, S.policy);
+            tma_load_2d_hint(d + kHalfTile, tk, 64, y, bar, S.policy);
+            tma_load_2d_hint(d + 2 * kHalfTile, tv, 0, y, bar, S.policy);
+            tma_load_2d_hint(d + 3 * kHalfTile, tv, 64, y, bar, S.policy);
+        }
+        __syncwarp();
         return true;
     };
     int n_req = 0, n_got = 0;   // chunks asked for, chunks received
@@ -382,15 +388,13 @@ __device__ __forceinline__ void produce(DecodeSmem& S, const DecodeArgs& a, cons
     int q = 0;
     for (; q < q_pre && ok; ++q) {
         if (q == claim_at && pool) request();
-        if (lane == 0) ok = issue(S.own[q], own_piece);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+        ok = issue(S.own[q], own_piece);
         ++k;
     }
     __syncthreads();   // the own part is described; every warp sees the barriers initialised
     for (; q < n_own && ok; ++q) {
         if (q == claim_at && pool) request();
-        if (lane == 0) ok = issue(S.own[q], own_piece);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+        ok = issue(S.own[q], own_piece);
         ++k;
     }
     int n = 0, buf = 0, piece = 0;
@@ -402,8 +406,7 @@ __device__ __forceinline__ void produce(DecodeSmem& S, const DecodeArgs& a, cons
         const int req_at = max(0, n - kClaimLead);
         for (int j = 0; j < n && ok; ++j) {
             if (j == req_at) request();
-            if (lane == 0) ok = issue(S.chunk[buf][j], piece);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
+            ok = issue(S.chunk[buf][j], piece);
             ++k;
         }
         if (ok) n = receive(buf, piece);

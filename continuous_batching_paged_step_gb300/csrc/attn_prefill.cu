@@ -80,17 +80,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-// True in exactly one lane of the (converged) warp.
-__device__ __forceinline__ bool elect_one() {
-    uint32_t p;
-    asm volatile(
-        "{\n\t.reg .pred P;\n\t"
-        "elect.sync _|P, 0xffffffff;\n\t"
-        "selp.b32 %0, 1, 0, P;\n\t}"
-        : "=r"(p));
-    return p != 0;
-}
-
 // Softmax and epilogue of one MMA tile (a warpgroup, one thread per row).
 __device__ __forceinline__ void softmax_tile(PrefillSmem& S, const PrefillArgs& a, uint32_t tmem, int t, int wq,
                                              int lane, int g, int row0, int qpos0, int ntok_t, int nt, int n_kt,
