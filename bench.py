@@ -325,8 +325,10 @@ def run_e2e(a, step, stream, dev, flush, dist, world):
     step's inputs go host -> device from pinned memory and its output device -> host,
     inside the timed region.  The copies are pipelined with the compute: two sets of
     device inputs/outputs, uploads on one stream, downloads on another, so step i+1's
-    upload and step i-1's download overlap step i's kernels.  No L2 flush here: every
-    step streams the decode rows' whole KV history (hundreds of MB, more than L2)."""
+    upload and step i-1's download overlap step i's kernels (and each other: an upload
+    waits only for the step that last read its input set, a step only for the download of
+    the output set it overwrites).  No L2 flush here: every step streams the decode rows'
+    whole KV history (hundreds of MB, more than L2)."""
     import torch
     from continuous_batching_paged_step_gb300 import kvpaged as kp
     from continuous_batching_paged_step_gb300 import replicas
@@ -342,7 +344,8 @@ def run_e2e(a, step, stream, dev, flush, dist, world):
     n = max(4, a.steps // 4)
 
     def run(count, timed):
-        done = [None] * count
+        done = [None] * count       # step i's output is on the host
+        computed = [None] * count   # step i's kernels finished (its input set is free)
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         if timed:
@@ -350,21 +353,23 @@ def run_e2e(a, step, stream, dev, flush, dist, world):
         for i in range(count):
             b = bufs[i % 2]
             if i >= 2:
-                up.wait_event(done[i - 2])          # the set is free once step i-2 finished
+                up.wait_event(computed[i - 2])      # step i-2 no longer reads this input set
             with torch.cuda.stream(up):
                 for nm in names:
                     b[nm].copy_(host[nm], non_blocking=True)
                 loaded = torch.cuda.Event()
                 loaded.record(up)
             stream.wait_event(loaded)
+            if i >= 2:
+                stream.wait_event(done[i - 2])      # step i-2's output left this output set
             kp.kv_append(step.pool.handle, b["k_new"], b["v_new"], b["cu_seqlens_q"], b["context_lens"],
                          b["block_tables"], stream=stream)
             kp.paged_attention_step(step.pool.handle, b["q"], outs[i % 2], b["cu_seqlens_q"], b["context_lens"],
                                     b["block_tables"], step.max_q_len, step.max_context_len, step.softmax_scale,
                                     step.workspace, stream=stream)
-            computed = torch.cuda.Event()
-            computed.record(stream)
-            down.wait_event(computed)
+            computed[i] = torch.cuda.Event()
+            computed[i].record(stream)
+            down.wait_event(computed[i])
             with torch.cuda.stream(down):
                 out_h[i % 2].copy_(outs[i % 2], non_blocking=True)
                 fin = torch.cuda.Event()
