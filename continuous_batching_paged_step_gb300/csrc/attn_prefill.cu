@@ -13,9 +13,10 @@
 // each block's (block, head g) 4 KiB tile is fetched by two 2-D TMA loads (one per 64-dim
 // half, 128-byte swizzle), landing in the canonical K-major SW128 layout.
 //
-// Warp roles (12 warps): warp 0 lane 0 issues the TMA loads of Q (once) and of K tiles
-// into a 3-stage ring, warp 2 lane 0 those of V tiles into a 2-stage ring; warp 1 owns TMEM (512 columns: S/P of tile A at 0, of B at 128, O of A
-// at 256, of B at 384) and lane 0 issues the MMAs; warps 4-7 run the softmax of tile A
+// Warp roles (12 warps): warp 0 issues the TMA loads of Q (once) and of K tiles into a
+// 3-stage ring, warp 2 those of V tiles into a 2-stage ring; warp 1 owns TMEM (512
+// columns: S/P of tile A at 0, of B at 128, O of A at 256, of B at 384) and issues the
+// MMAs (the warp in step, one elected lane issuing); warps 4-7 run the softmax of tile A
 // and warps 8-11 that of tile B, one thread per MMA row (TMEM lane).  The MMA warp
 // ping-pongs: O_A += P_A V_kt, S_A = Q_A K_{kt+1}^T, O_B += P_B V_kt, S_B = ..., so the
 // softmax of one tile runs while the tensor core works on the other.  Per key tile a
