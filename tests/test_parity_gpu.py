@@ -104,6 +104,24 @@ def test_decode_ranges_beyond_staged_ids(runner, ctas):
     _run_full_check(runner, spec, ctas=ctas)
 
 
+def test_many_requests(runner):
+    # 5,000 requests, more than every per-step staging capacity: kv_append's and the decode
+    # kernel's shared-memory copies of the step metadata (2,048 requests) fall back to global
+    # memory, and the combine kernel's CTA pairs each plan more than one round of rows.
+    # Mostly short decode rows (1-3 blocks, so nearly every row is split across pieces),
+    # a few empty requests and two prefill chunks.
+    rng = np.random.default_rng(9090)
+    n = 5000
+    q_lens = [1] * n
+    ctx = [int(c) for c in rng.integers(0, 48, size=n)]
+    for i in rng.choice(n, size=40, replace=False):
+        q_lens[i] = 0
+    q_lens[1234], ctx[1234] = 70, 19
+    q_lens[4321], ctx[4321] = 40, 0
+    spec = wl.StepSpec("many-requests", q_lens=q_lens, ctx_lens=ctx, num_blocks=12288, seed=9091)
+    _run_full_check(runner, spec)
+
+
 def test_edge_cases(runner):
     # an empty request in the middle, decode at positions 0 / 15 / 16 / 31 / 32 / 8192,
     # prefill of 2 rows, a 33-row chunk (two q tiles, one row in the second), a chunk whose
