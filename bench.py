@@ -438,9 +438,13 @@ def run_reference(a):
 def run_trace(a):
     """The trace replay: 512 requests (Poisson arrivals, shared 1024-token system prompt in
     refcounted blocks, lognormal prompts and outputs), FCFS under an 8192-token budget, a
-    40 GiB pool; every step is kv_append + paged_attention_step.  Reports packed tokens
-    over the summed GPU time of the steps (host scheduling and input generation are not
-    timed), the per-step distribution, and the decode KV bytes streamed."""
+    40 GiB pool; every step is kv_append + paged_attention_step.  The trace is served once
+    as the Python driver runs it (it plans each step and draws its inputs on the host,
+    slower than the GPU step: those step windows are reported as `served`), recording
+    every step's device inputs and block-manager calls; the headline value then serves the
+    recorded steps again on a fresh pool, back to back, with the inputs resident in HBM
+    (packed tokens over the GPU time of the whole replay).  A second replay with events
+    around every kernel gives the per-kernel split."""
     import torch
     from continuous_batching_paged_step_gb300 import build as b
     b.build()
@@ -448,45 +452,40 @@ def run_trace(a):
     from continuous_batching_paged_step_gb300 import workloads as wl
     from continuous_batching_paged_step_gb300.trace import TraceRunner
     ts = wl.TraceSpec()
-    # headline replay: steps as served (no events inside the library calls)
     tr = TraceRunner(ts)
     w0 = time.perf_counter()
-    tr.run()
+    tr.run(record=True)
     wall = time.perf_counter() - w0
     st = kp.kv_pool_get_error(tr.pool.handle)
     if st != (0, 0):
         raise RuntimeError(f"device error word after the trace: {st}")
-    s = tr.summary()
+    served = tr.summary()
+    rep = tr.replay()
+    rep_ev = tr.replay(timing_launches=8 * 4000)
     tr.close()
-    # the same replay again with events around every kernel, for the per-kernel split
-    tr = TraceRunner(ts)
-    kp.kv_pool_enable_timing(tr.pool.handle, 8 * 4000)
-    tr.run()
-    per_kernel = kp.kv_pool_read_timing(tr.pool.handle)
-    kp.kv_pool_enable_timing(tr.pool.handle, 0)
-    s_ev = tr.summary()
+    per_kernel = rep_ev["kernels"]
     hbm, bf16, _, peak_src = peaks()
     n_dec, ms_dec = per_kernel["decode_splitkv"]
-    dec_gbs = s["decode_bytes"] / (ms_dec / 1e3) / 1e9 if ms_dec else None
-    line = {"metric": METRIC, "value": round(s["tokens_per_s"], 1), "unit": UNIT, "n_gpus": 1, "steps": s["steps"],
-            "warmup": 0, "ms_per_step": round(s["gpu_ms"] / max(1, s["steps"]), 5), "higher_is_better": True,
+    dec_gbs = served["decode_bytes"] / (ms_dec / 1e3) / 1e9 if ms_dec else None
+    line = {"metric": METRIC, "value": round(rep["tokens_per_s"], 1), "unit": UNIT, "n_gpus": 1, "steps": rep["steps"],
+            "warmup": 0, "ms_per_step": round(rep["gpu_ms"] / max(1, rep["steps"]), 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": ts.name, "requests": ts.n_requests, "shared_prefix": ts.shared_prefix,
                        "budget": ts.budget, "kv_pool_blocks": ts.pool_blocks,
                        "arrivals_per_step": ts.arrivals_per_step,
-                       "l2": "not flushed: consecutive steps back to back, as served"},
-            "trace": {k: (round(v, 4) if isinstance(v, float) else v) for k, v in s.items()},
+                       "l2": "not flushed: consecutive steps back to back, as served",
+                       "timed": "recorded steps replayed back to back (inputs in HBM, block-manager calls between steps)"},
+            "replay": {k: (round(v, 4) if isinstance(v, float) else v) for k, v in rep.items()},
+            "served": {k: (round(v, 4) if isinstance(v, float) else v) for k, v in served.items()},
+            # decode GB/s counts every request's shared-prefix blocks once per read, as the
+            # algorithm reads them; they are the same physical blocks (L2-resident), so this
+            # may exceed the HBM rate
             "decode_kv_gbs": round(dec_gbs, 1) if dec_gbs else None,
-            "decode_kv_frac_of_hbm": round(dec_gbs / hbm, 4) if dec_gbs else None,
             "kernels_ms_total": {k: round(v[1], 3) for k, v in per_kernel.items() if v[0]},
-            "gpu_ms_with_kernel_events": round(s_ev["gpu_ms"], 3),
-            # the step windows include the time the GPU waits for this Python driver to
-            # launch the step (its planning and input generation are slower than the GPU);
-            # tokens over the summed kernel durations bound what the kernels alone sustain
-            "kernel_busy_tokens_per_s": round(s["tokens"] / (sum(v[1] for v in per_kernel.values()) / 1e3), 1),
+            "gpu_ms_with_kernel_events": round(rep_ev["gpu_ms"], 3),
+            "kernel_busy_tokens_per_s": round(rep["tokens"] / (sum(v[1] for v in per_kernel.values()) / 1e3), 1),
             "wall_s": round(wall, 1)}
     print(json.dumps(line), flush=True)
-    tr.close()
 
 
 def main():

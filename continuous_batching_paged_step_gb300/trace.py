@@ -165,7 +165,13 @@ def history(ts: TraceSpec, rs: RunState):
 
 
 class TraceRunner:
-    """Runs a trace on the GPU: every step is kv_append + paged_attention_step."""
+    """Runs a trace on the GPU: every step is kv_append + paged_attention_step.
+
+    `run(record=True)` also keeps every step's device inputs and the block-manager calls
+    made around it, so that `replay()` can serve the same steps again, back to back, on a
+    fresh pool: the scheduling and the input generation (host work, slower than the GPU
+    step) are then out of the timed loop, as in a serving engine that plans step n + 1
+    while the GPU runs step n."""
 
     def __init__(self, ts: TraceSpec, device="cuda", max_reqs: int | None = None):
         import torch
@@ -188,13 +194,29 @@ class TraceRunner:
         self.out = torch.empty((T, 4096), dtype=torch.bfloat16, device=device)
         self.ws = torch.empty(kp.paged_attention_workspace_size(h, self.max_reqs, T, longest), dtype=torch.uint8,
                               device=device)
-        self.sched = Scheduler(self.trace, ts, self.shared_blocks, lambda n: kp.kv_block_alloc(h, n),
-                               lambda ids: kp.kv_block_ref(h, ids), lambda ids: kp.kv_block_free(h, ids))
+        self._log = None   # block-manager calls of the current step, while recording
+        self.sched = Scheduler(self.trace, ts, self.shared_blocks, self._alloc, self._ref, self._free)
         self._write_shared_prefix()
         self.step_ms = []
         self.step_tokens = []
         self.step_decode_bytes = []
         self.checks = []
+
+    def _alloc(self, n):
+        ids = self.kp.kv_block_alloc(self.pool.handle, n)
+        if self._log is not None:
+            self._log.append(("alloc", [int(b) for b in ids]))
+        return ids
+
+    def _ref(self, ids):
+        self.kp.kv_block_ref(self.pool.handle, ids)
+        if self._log is not None:
+            self._log.append(("ref", [int(b) for b in ids]))
+
+    def _free(self, ids):
+        self.kp.kv_block_free(self.pool.handle, ids)
+        if self._log is not None:
+            self._log.append(("free", [int(b) for b in ids]))
 
     def _write_shared_prefix(self):
         torch, kp = self.torch, self.kp
@@ -217,19 +239,27 @@ class TraceRunner:
                 np.concatenate([p[2] for p in parts]))
 
     def run(self, max_steps: int | None = None, check_every: int = 0, check_rows: int = 4, oracle=None,
-            on_check=None):
+            on_check=None, record: bool = False):
         """Replay the trace.  With check_every > 0, every check_every-th step a few rows are
         compared against `oracle` (a callable taking (q rows, K histories, V histories,
-        cu, ctx) and returning fp64 outputs) through `on_check(step, got, want)`."""
+        cu, ctx) and returning fp64 outputs) through `on_check(step, got, want)`.  With
+        record, every step is kept for `replay()`."""
         torch, kp = self.torch, self.kp
         dev = self.device
         stream = torch.cuda.current_stream(dev)
         evs = []
         h = self.pool.handle
+        if record:
+            self.recorded = []
         while not self.sched.finished() and (max_steps is None or self.sched.step < max_steps):
+            pre = self._log = [] if record else None
             plan = self.sched.plan()
             if not plan.entries:
+                post = self._log = [] if record else None
                 self.sched.commit(plan)
+                self._log = None
+                if record:
+                    self.recorded.append({"pre": pre, "post": post, "T": 0})
                 continue
             R, T = len(plan.entries), plan.num_tokens
             if R > self.max_reqs:
@@ -254,6 +284,10 @@ class TraceRunner:
             evs.append((e0, e1))
             self.step_tokens.append(T)
             self.step_decode_bytes.append(sum(4096 * (c + 1) for (_, c, qq) in plan.entries if qq == 1))
+            if record:
+                self.recorded.append({"pre": pre, "T": T, "q": self.q[:T].clone(), "k": self.k_new[:T].clone(),
+                                      "v": self.v_new[:T].clone(), "cu": cu_d, "ctx": ctx_d, "tab": tab_d,
+                                      "max_q": int(max(cu[1:] - cu[:-1])), "max_ctx": int(ctx.max())})
             if check_every and oracle is not None and plan.step % check_every == 0:
                 torch.cuda.synchronize(dev)
                 got = self.out[:T].float().cpu().numpy().reshape(T, 32, 128)
@@ -273,10 +307,81 @@ class TraceRunner:
                 sel = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in pick])
                 on_check(plan.step, got[sel], want)
                 self.checks.append(plan.step)
+            post = self._log = [] if record else None
             self.sched.commit(plan)
+            self._log = None
+            if record:
+                self.recorded[-1]["post"] = post
         torch.cuda.synchronize(dev)
         self.step_ms = [a.elapsed_time(b) for a, b in evs]
         return self
+
+    def replay(self, timing_launches: int = 0) -> dict:
+        """Serve the recorded steps again on a fresh pool, back to back: per step the
+        block-manager calls made before it (runs of one kind merged into one call: the
+        allocator hands out and takes back ids in call order), kv_append and
+        paged_attention_step on the recorded device inputs, then the calls made after it.
+        Returns the tokens and the GPU time of the whole replay (one pair of events around
+        it, so host time between steps counts when the GPU waits for it).  With
+        timing_launches > 0 the library also times each of its kernel launches (events
+        around each, which stops their overlap) and the result holds the per-kernel sums."""
+        torch, kp = self.torch, self.kp
+        dev = self.device
+        stream = torch.cuda.current_stream(dev)
+        shared = list(self.shared_blocks)
+        self.pool.close()
+        self.pool = kp.KVPool(self.ts.pool_blocks, device=dev)
+        h = self.pool.handle
+        got = [int(b) for b in kp.kv_block_alloc(h, len(shared))]
+        if got != shared:
+            raise RuntimeError("replay: the fresh pool handed out other shared-prefix blocks")
+        self._write_shared_prefix()
+        if timing_launches:
+            kp.kv_pool_enable_timing(h, timing_launches)
+
+        def apply(ops):
+            i = 0
+            while i < len(ops):
+                kind, ids = ops[i][0], list(ops[i][1])
+                j = i + 1
+                while j < len(ops) and ops[j][0] == kind:
+                    ids += ops[j][1]
+                    j += 1
+                if kind == "alloc":
+                    if [int(b) for b in kp.kv_block_alloc(h, len(ids))] != ids:
+                        raise RuntimeError("replay: the allocator handed out other blocks than recorded")
+                elif kind == "ref":
+                    kp.kv_block_ref(h, ids)
+                else:
+                    kp.kv_block_free(h, ids)
+                i = j
+
+        scale = 1.0 / math.sqrt(128.0)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tokens = 0
+        e0.record(stream)
+        for rec in self.recorded:
+            apply(rec["pre"])
+            T = rec["T"]
+            if T:
+                kp.kv_append(h, rec["k"], rec["v"], rec["cu"], rec["ctx"], rec["tab"])
+                kp.paged_attention_step(h, rec["q"], self.out[:T], rec["cu"], rec["ctx"], rec["tab"], rec["max_q"],
+                                        rec["max_ctx"], scale, self.ws)
+                tokens += T
+            apply(rec["post"])
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1)
+        res = {"steps": sum(1 for r in self.recorded if r["T"]), "tokens": tokens, "gpu_ms": ms,
+               "tokens_per_s": tokens / (ms / 1e3) if ms > 0 else 0.0}
+        if timing_launches:
+            res["kernels"] = kp.kv_pool_read_timing(h)
+            kp.kv_pool_enable_timing(h, 0)
+        st = kp.kv_pool_get_error(h)
+        if st != (0, 0):
+            raise RuntimeError(f"replay: device error word {st}")
+        return res
 
     def summary(self) -> dict:
         ms = np.array(self.step_ms)

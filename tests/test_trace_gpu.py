@@ -44,3 +44,30 @@ def test_short_trace_against_oracle():
         assert all(kp.kv_block_refcount(tr.pool.handle, b) == 1 for b in tr.shared_blocks)
     finally:
         tr.close()
+
+
+def test_replay_matches_the_served_run():
+    # The recorded steps served again on a fresh pool (the benchmark's timed replay) give
+    # bit-identical outputs, hand out the same blocks and leave the pool as the served run did.
+    from continuous_batching_paged_step_gb300 import build
+    build.build()
+    import torch
+    from continuous_batching_paged_step_gb300 import kvpaged as kp
+    from continuous_batching_paged_step_gb300.trace import TraceRunner
+    ts = wl.TraceSpec(name="short-replay", n_requests=30, arrivals_per_step=3.0, shared_prefix=32, prompt_median=50,
+                      prompt_cap=300, output_median=12, output_range=(10, 30), budget=192, pool_blocks=2048, seed=33)
+    tr = TraceRunner(ts)
+    try:
+        tr.run(max_steps=25, record=True)
+        last = max(i for i, r in enumerate(tr.recorded) if r["T"])
+        T = tr.recorded[last]["T"]
+        served_out = tr.out[:T].clone()
+        free_served = kp.kv_pool_num_free(tr.pool.handle)
+        res = tr.replay()
+        torch.cuda.synchronize()
+        assert res["steps"] == sum(1 for r in tr.recorded if r["T"])
+        assert res["tokens"] == sum(r["T"] for r in tr.recorded)
+        assert torch.equal(tr.out[:T].view(torch.int16), served_out.view(torch.int16))
+        assert kp.kv_pool_num_free(tr.pool.handle) == free_served
+    finally:
+        tr.close()
