@@ -3,7 +3,8 @@
 
 One step = one pass of the hot path over one packed batch: kv_append of the step's new
 K/V rows into the 16-token block pool, then paged_attention_step (metadata prep,
-tcgen05 prefill tiles, split-KV decode with in-kernel merge), all through the C ABI.
+tcgen05 prefill tiles beside the split-KV decode, then the combine of split rows), all
+through the C ABI.
 
 Metric: packed query tokens/s per attention layer (T / step time), and the decode
 kernel's KV-read GB/s against the measured HBM peak.  Default workload: the mixed
