@@ -701,7 +701,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
 constexpr int kCombineHeads = kNumQHeads / 2;         // query heads of one combine CTA (half a row)
 constexpr int kCombineThreads = kCombineHeads * 32;   // one warp per query head
-constexpr int kCombineStageMax = 12;                  // pieces staged in shared memory at once (at most)
+constexpr int kCombineStage = 12;                     // pieces staged in shared memory at once
+constexpr int kCombineStageWide = 20;                 // ... when every row's CTA pair has an SM pair to itself
 constexpr int kCombineAccBytes = kCombineHeads * kHeadDim * 4;   // one piece's accumulators: 8 KiB
 constexpr int kCombineMlBytes = kCombineHeads * 8;               // one piece's (m, l): 128 B
 
@@ -880,12 +881,16 @@ cudaError_t launch_decode(const StepArgs& a, const CUtensorMap* tmap_k, const CU
 cudaError_t launch_combine(const StepArgs& a, cudaStream_t stream) {
     const StepLayout& L = a.lay;
     const int wave = decode_wave(a);
-    // Two CTAs per row, and no more CTAs than run at once (two per SM, each staging up to
-    // 12 pieces), each pair then taking several rows.  (Three CTAs per SM staging 8 pieces
-    // each merged the 256-row decode step more slowly: its longest rows took more rounds.)
-    const int stage = kCombineStageMax;
+    // Two CTAs per row, and no more CTAs than run at once, each pair then taking several
+    // rows.  When there are at most as many rows as SM pairs, each CTA gets an SM to itself
+    // and stages 20 pieces at once (one round trip for the long rows of a mixed step);
+    // otherwise two CTAs per SM stage 12 each.  (Three CTAs per SM staging 8 pieces each
+    // merged the 256-row decode step more slowly: its longest rows took more rounds.)
+    const long long sms = a.num_sms > 0 ? a.num_sms : 1;
+    const bool wide = 2LL * a.num_reqs <= sms;
+    const int stage = wide ? kCombineStageWide : kCombineStage;
     long long grid = 2LL * a.num_reqs;
-    const long long cap = 2LL * (a.num_sms > 0 ? a.num_sms : 1);
+    const long long cap = wide ? sms / 2 * 2 : 2LL * sms;
     if (grid > cap) grid = cap;
     if (grid < 2) grid = 2;
     return launch_pdl(combine_kernel, dim3((unsigned)grid), dim3(kCombineThreads), combine_smem_bytes(stage), stream,
@@ -901,7 +906,7 @@ cudaError_t configure_decode_kernel() {
                                                (int)(sizeof(DecodeSmem) + 1024));
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)combine_smem_bytes(kCombineStageMax));
+                                (int)combine_smem_bytes(kCombineStageWide));
 }
 
 }  // namespace kvp
