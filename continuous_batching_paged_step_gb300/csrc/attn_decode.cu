@@ -797,6 +797,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const int32_t*
                                   pol);
                     }
                 }
+                // thread 0's warp waits on the barrier together, once the copies are out (lanes
+                // of that warp that waited on it while thread 0 was held up elsewhere went on
+                // before the copies had landed)
+                __syncwarp();
                 if (!mbar_wait(&S.full, phase)) {
                     // the copies did not land within the wait limit; they target this CTA's shared
                     // memory, so give them another bounded wait before leaving
