@@ -172,20 +172,26 @@ def oracle_sample_rows(spec, rows_per_chunk):
 _ORACLE_INPUTS = {}
 
 
-def time_oracle(config, rows_per_chunk):
+def time_oracle(config, rows_per_chunk, min_seconds=0.0):
     """Wall time of the oracle (one process, BLAS limited to one thread at start-up) over
-    a sample of the step's rows.  Input generation is outside the timed call."""
+    a sample of the step's rows, repeated until at least `min_seconds` have been timed.
+    Returns (rows computed, wall seconds, passes).  Input generation is outside the timed
+    calls."""
     import oracle
     from continuous_batching_paged_step_gb300 import workloads as wl
     if config not in _ORACLE_INPUTS:
         _ORACLE_INPUTS[config] = wl.make_inputs(wl.CONFIGS[config]())
     inp = _ORACLE_INPUTS[config]
     rows = oracle_sample_rows(inp.spec, rows_per_chunk)
-    t0 = time.perf_counter()
-    out = oracle.step_reference(inp, rows=rows)
-    wall = time.perf_counter() - t0
-    assert np.isfinite(out[rows]).all()
-    return len(rows), wall
+    n, wall, passes = 0, 0.0, 0
+    while passes == 0 or wall < min_seconds:
+        t0 = time.perf_counter()
+        out = oracle.step_reference(inp, rows=rows)
+        wall += time.perf_counter() - t0
+        assert np.isfinite(out[rows]).all()
+        n += len(rows)
+        passes += 1
+    return n, wall, passes
 
 
 # ---------------------------------------------------------------------- GPU arm
@@ -296,11 +302,11 @@ def run_gpu(a):
 
     cpu = None
     if not a.no_cpu_baseline:
-        n_rows, owall = time_oracle(a.config, a.oracle_rows_per_chunk)
+        n_rows, owall, passes = time_oracle(a.config, a.oracle_rows_per_chunk, a.oracle_seconds)
         cpu = {"value": round(n_rows / owall, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n_rows} of {T} packed rows of the {spec.name} step (every decode row, "
-                         f"{a.oracle_rows_per_chunk} evenly spaced rows per prefill chunk), fp64 numpy, "
-                         f"one process, {owall:.1f} s"}
+               "sample": f"{passes} passes over {n_rows // passes} of {T} packed rows of the {spec.name} step "
+                         f"(every decode row, {a.oracle_rows_per_chunk} evenly spaced rows per prefill chunk), "
+                         f"fp64 numpy, one process, {owall:.1f} s"}
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": a.steps,
@@ -412,13 +418,13 @@ def run_reference(a):
     budget_s = 150.0
     # first timed probe with a small sample, then size the per-step sample to the budget
     rows_per_chunk = 4
-    n_rows, w = time_oracle(a.config, rows_per_chunk)
+    n_rows, w, _ = time_oracle(a.config, rows_per_chunk)
     per_step_target = budget_s / max(1, a.steps + a.warmup)
     if w < per_step_target / 2:
         rows_per_chunk = int(min(max(spec.q_lens), rows_per_chunk * per_step_target / max(w, 1e-3)))
     times = []
     for i in range(a.warmup + a.steps):
-        n_rows, w = time_oracle(a.config, rows_per_chunk)
+        n_rows, w, _ = time_oracle(a.config, rows_per_chunk)
         if i >= a.warmup:
             times.append(w)
     per = statistics.median(times)
@@ -498,6 +504,8 @@ def main():
     p.add_argument("--config", choices=["mixed", "decode", "chunked", "tiny", "trace"], default="mixed")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--oracle-rows-per-chunk", type=int, default=256)
+    p.add_argument("--oracle-seconds", type=float, default=10.0,
+                   help="the cpu_baseline repeats its sample until this much oracle time is measured")
     a = p.parse_args()
     if a.warmup < 3:
         p.error("--warmup must be at least 3")
