@@ -341,47 +341,64 @@ def run_e2e(a, step, stream, dev, flush, dist, world):
     from continuous_batching_paged_step_gb300 import replicas
     inp = step.inp
     names = ("q", "k_new", "v_new", "cu_seqlens_q", "context_lens", "block_tables")
-    host = {n: getattr(step, n).cpu().pin_memory() for n in names}
+    # the step's inputs packed into one pinned host blob (each at a 256-byte offset), so that
+    # a step's upload is one copy; the device sets hold the same layout, viewed per input
+    offs, total_bytes = {}, 0
+    for nm in names:
+        t = getattr(step, nm)
+        offs[nm] = total_bytes
+        total_bytes += (t.numel() * t.element_size() + 255) & ~255
+
+    def views(blob):
+        out = {}
+        for nm in names:
+            t = getattr(step, nm)
+            nb = t.numel() * t.element_size()
+            out[nm] = blob[offs[nm]:offs[nm] + nb].view(t.dtype).view(t.shape)
+        return out
+
+    host_blob = torch.empty(total_bytes, dtype=torch.uint8).pin_memory()
+    for nm, v in views(host_blob).items():
+        v.copy_(getattr(step, nm).cpu())
+    dev_blobs = [torch.empty(total_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    bufs = [views(b) for b in dev_blobs]
     out_h = [torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory() for _ in range(2)]
-    bufs = [{n: torch.empty_like(getattr(step, n)) for n in names} for _ in range(2)]
     outs = [torch.empty_like(step.out) for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = total_bytes
     d2h = out_h[0].numel() * out_h[0].element_size()
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     n = max(4, a.steps // 4)
+    # events reused by parity: step i waits on those step i - 2 recorded, before it records its own
+    loaded = torch.cuda.Event()
+    computed = [torch.cuda.Event() for _ in range(2)]   # step's kernels finished (its input set is free)
+    done = [torch.cuda.Event() for _ in range(2)]       # step's output is on the host
 
     def run(count, timed):
-        done = [None] * count       # step i's output is on the host
-        computed = [None] * count   # step i's kernels finished (its input set is free)
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         if timed:
             t0.record(up)
         for i in range(count):
-            b = bufs[i % 2]
+            j = i % 2
+            b = bufs[j]
             if i >= 2:
-                up.wait_event(computed[i - 2])      # step i-2 no longer reads this input set
+                up.wait_event(computed[j])          # step i-2 no longer reads this input set
             with torch.cuda.stream(up):
-                for nm in names:
-                    b[nm].copy_(host[nm], non_blocking=True)
-                loaded = torch.cuda.Event()
+                dev_blobs[j].copy_(host_blob, non_blocking=True)
                 loaded.record(up)
             stream.wait_event(loaded)
             if i >= 2:
-                stream.wait_event(done[i - 2])      # step i-2's output left this output set
+                stream.wait_event(done[j])          # step i-2's output left this output set
             kp.kv_append(step.pool.handle, b["k_new"], b["v_new"], b["cu_seqlens_q"], b["context_lens"],
                          b["block_tables"], stream=stream)
-            kp.paged_attention_step(step.pool.handle, b["q"], outs[i % 2], b["cu_seqlens_q"], b["context_lens"],
+            kp.paged_attention_step(step.pool.handle, b["q"], outs[j], b["cu_seqlens_q"], b["context_lens"],
                                     b["block_tables"], step.max_q_len, step.max_context_len, step.softmax_scale,
                                     step.workspace, stream=stream)
-            computed[i] = torch.cuda.Event()
-            computed[i].record(stream)
-            down.wait_event(computed[i])
+            computed[j].record(stream)
+            down.wait_event(computed[j])
             with torch.cuda.stream(down):
-                out_h[i % 2].copy_(outs[i % 2], non_blocking=True)
-                fin = torch.cuda.Event()
-                fin.record(down)
-            done[i] = fin
+                out_h[j].copy_(outs[j], non_blocking=True)
+                done[j].record(down)
         if timed:
             t1.record(down)
         torch.cuda.synchronize(dev)
@@ -392,7 +409,8 @@ def run_e2e(a, step, stream, dev, flush, dist, world):
     T = inp.spec.num_tokens
     return {"value": round(replicas.aggregate_rate(T * n, world, total), 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,
-            "pipelining": "double-buffered device inputs/outputs; uploads, kernels and downloads on three streams"}
+            "pipelining": "double-buffered device inputs/outputs, each step's inputs one packed upload; "
+                          "uploads, kernels and downloads on three streams"}
 
 
 # ---------------------------------------------------------------- reference arm

@@ -64,7 +64,7 @@ constexpr int kStageBytes = 4 * kHalfTile;             // K and V, two halves ea
 
 constexpr int kIdCap = 1024;       // blocks of a CTA's range (its own part is staged up front)
 constexpr int kTailPercent = 20;   // share of each range handed out as chunks
-constexpr int kChunkTarget = 4;    // blocks per chunk, at least
+constexpr int kChunkTarget = 8;    // blocks per chunk, at least (fewer pieces to merge; 4 and 6 measured slower)
 constexpr int kMaxPieces = 8;      // pieces per range: own part + chunks
 constexpr int kMaxChunk = 32;      // blocks per chunk, at most (one scheduler lane each)
 constexpr int kClaimLead = 3;      // blocks still to issue (own part or chunk) when the next chunk is claimed
@@ -185,7 +185,7 @@ __device__ __forceinline__ Layout make_layout(int P, int G) {
 // linearly: chunk k (0-based) gets a share n_ch - k of n_ch (n_ch + 1) / 2, so the last
 // chunks handed out are the smallest and the CTAs that take them finish close together.
 // The tail holds at least n_ch (n_ch + 1) / 2 blocks (so that no chunk is empty: make_layout
-// keeps 4 n_ch <= n / 5 and n_ch <= 7) and at most 16 pp (so that the first, largest chunk
+// keeps kChunkTarget n_ch <= n / 5 and n_ch <= 7) and at most 16 pp (so that the first, largest chunk
 // has at most 2 tail / pp <= kMaxChunk blocks).
 __device__ __forceinline__ int tail_blocks(const Layout& L, int n) {
     return L.pp > 1 ? min(n * kTailPercent / 100, 16 * L.pp) : 0;
