@@ -156,23 +156,20 @@ class ClockSampler:
 
 # --------------------------------------------------------------------- oracle leg
 
-def oracle_sample_rows(spec, rows_per_chunk):
-    """Every decode row plus `rows_per_chunk` evenly spaced rows of each prefill chunk."""
-    cu = np.concatenate([[0], np.cumsum(spec.q_lens)]).astype(int)
-    rows = []
-    for r, q in enumerate(spec.q_lens):
-        if q == 1:
-            rows.append(int(cu[r]))
-        elif q > 1:
-            k = min(q, rows_per_chunk)
-            rows += sorted(set(int(cu[r] + j) for j in np.linspace(0, q - 1, k).round().astype(int)))
-    return np.array(rows, dtype=np.int64)
+def oracle_sample_rows(T, n_rows, shift=0):
+    """n_rows packed rows evenly spaced over the whole step (every row when n_rows >= T), so
+    decode rows and prefill rows at every position enter in proportion and the oracle's
+    rows/s stands for the whole step's.  Sample `shift` starts at a golden-ratio fraction of
+    the spacing, so that successive samples cover all rows."""
+    n = max(1, min(T, int(n_rows)))
+    frac = (shift * 0.6180339887498949) % 1.0
+    return np.unique(np.minimum(((np.arange(n) + frac) * (T / n)).astype(np.int64), T - 1))
 
 
 _ORACLE_INPUTS = {}
 
 
-def time_oracle(config, rows_per_chunk, min_seconds=0.0):
+def time_oracle(config, n_rows, min_seconds=0.0, shift=0):
     """Wall time of the oracle (one process, BLAS limited to one thread at start-up) over
     a sample of the step's rows, repeated until at least `min_seconds` have been timed.
     Returns (rows computed, wall seconds, passes).  Input generation is outside the timed
@@ -182,9 +179,9 @@ def time_oracle(config, rows_per_chunk, min_seconds=0.0):
     if config not in _ORACLE_INPUTS:
         _ORACLE_INPUTS[config] = wl.make_inputs(wl.CONFIGS[config]())
     inp = _ORACLE_INPUTS[config]
-    rows = oracle_sample_rows(inp.spec, rows_per_chunk)
     n, wall, passes = 0, 0.0, 0
     while passes == 0 or wall < min_seconds:
+        rows = oracle_sample_rows(inp.spec.num_tokens, n_rows, shift + passes)
         t0 = time.perf_counter()
         out = oracle.step_reference(inp, rows=rows)
         wall += time.perf_counter() - t0
@@ -302,11 +299,15 @@ def run_gpu(a):
 
     cpu = None
     if not a.no_cpu_baseline:
-        n_rows, owall, passes = time_oracle(a.config, a.oracle_rows_per_chunk, a.oracle_seconds)
+        # a short probe sizes the sample: as many evenly spaced rows as one pass of about
+        # oracle_seconds allows (the whole step when it fits), repeated up to that time
+        n_probe, w_probe, _ = time_oracle(a.config, 32)
+        n_pass = min(T, max(32, int(n_probe / max(w_probe, 1e-6) * a.oracle_seconds)))
+        n_rows, owall, passes = time_oracle(a.config, n_pass, a.oracle_seconds)
         cpu = {"value": round(n_rows / owall, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{passes} passes over {n_rows // passes} of {T} packed rows of the {spec.name} step "
-                         f"(every decode row, {a.oracle_rows_per_chunk} evenly spaced rows per prefill chunk), "
-                         f"fp64 numpy, one process, {owall:.1f} s"}
+               "sample": f"{passes} pass(es) over {n_rows // passes} of {T} packed rows of the {spec.name} step, "
+                         f"evenly spaced over the step (decode and prefill rows in proportion), fp64 numpy, "
+                         f"one process, {owall:.1f} s"}
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": a.steps,
@@ -435,20 +436,21 @@ def run_reference(a):
     workers = 1
     budget_s = 150.0
     # first timed probe with a small sample, then size the per-step sample to the budget
-    rows_per_chunk = 4
-    n_rows, w, _ = time_oracle(a.config, rows_per_chunk)
+    # (at least 16 evenly spaced rows a step)
+    n_probe, w, _ = time_oracle(a.config, 32)
     per_step_target = budget_s / max(1, a.steps + a.warmup)
-    if w < per_step_target / 2:
-        rows_per_chunk = int(min(max(spec.q_lens), rows_per_chunk * per_step_target / max(w, 1e-3)))
-    times = []
+    n_pass = min(spec.num_tokens, max(8, int(n_probe / max(w, 1e-6) * per_step_target)))
+    rows_timed, t_timed = 0, 0.0
     for i in range(a.warmup + a.steps):
-        n_rows, w, _ = time_oracle(a.config, rows_per_chunk)
+        n_rows, w, _ = time_oracle(a.config, n_pass, shift=i)
         if i >= a.warmup:
-            times.append(w)
-    per = statistics.median(times)
-    value = n_rows / per
-    sample = (f"{n_rows} of {spec.num_tokens} packed rows per step of the {spec.name} step (every decode row, "
-              f"{rows_per_chunk} evenly spaced rows per prefill chunk)")
+            rows_timed += n_rows
+            t_timed += w
+    per = t_timed / max(1, a.steps)
+    value = rows_timed / max(t_timed, 1e-9)
+    sample = (f"{n_pass} of {spec.num_tokens} packed rows per step of the {spec.name} step, evenly spaced over "
+              f"the step (decode and prefill rows in proportion, shifted from step to step); value = rows / time "
+              f"over the timed steps")
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(per * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
@@ -521,7 +523,6 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", choices=["mixed", "decode", "chunked", "tiny", "trace"], default="mixed")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--oracle-rows-per-chunk", type=int, default=256)
     p.add_argument("--oracle-seconds", type=float, default=10.0,
                    help="the cpu_baseline repeats its sample until this much oracle time is measured")
     a = p.parse_args()

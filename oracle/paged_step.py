@@ -213,8 +213,9 @@ def attention_dense_mask(q, k_prior, v_prior, k_new, v_new, cu_seqlens_q, contex
 
 # ----------------------------------------------------------------- full-step helpers
 
-def request_histories(inp):
-    """Contiguous K and V history of every request: cached tokens then this step's rows.
+def request_histories(inp, requests=None):
+    """Contiguous K and V history of every request (or of the listed ones; None for the
+    others): cached tokens then this step's rows.
 
     `inp` is a StepInputs from the seeded generator.
     """
@@ -223,7 +224,7 @@ def request_histories(inp):
     for r in range(len(inp.context_lens)):
         s, e = int(cu[r]), int(cu[r + 1])
         kp, vp = inp.k_prior[r], inp.v_prior[r]
-        if kp is None:
+        if kp is None or (requests is not None and r not in requests):
             ks.append(None)
             vs.append(None)
             continue
@@ -235,7 +236,11 @@ def request_histories(inp):
 def step_reference(inp, rows=None, softmax_scale=None):
     """Attention output of one whole step (or of the listed rows), fp64 [T, n_q, d]."""
     spec = inp.spec
-    ks, vs = request_histories(inp)
+    needed = None
+    if rows is not None:   # only the requests that own a listed row
+        cu = np.asarray(inp.cu_seqlens_q)
+        needed = set(int(r) for r in np.searchsorted(cu, np.asarray(list(rows), dtype=np.int64), side="right") - 1)
+    ks, vs = request_histories(inp, needed)
     return attention_reference(inp.q, ks, vs, inp.cu_seqlens_q, inp.context_lens,
                                spec.n_q_heads, spec.n_kv_heads, spec.head_dim,
                                softmax_scale=softmax_scale, rows=rows)
