@@ -699,31 +699,33 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     } else consume(S, b, L, warp, lane);
 }
 
-constexpr int kCombineHeads = kNumQHeads / 2;         // query heads of one combine CTA (half a row)
-constexpr int kCombineThreads = kCombineHeads * 32;   // one warp per query head
 constexpr int kCombineStage = 12;                     // pieces staged in shared memory at once
-constexpr int kCombineStageWide = 20;                 // ... when every row's CTA pair has an SM pair to itself
-constexpr int kCombineAccBytes = kCombineHeads * kHeadDim * 4;   // one piece's accumulators: 8 KiB
-constexpr int kCombineMlBytes = kCombineHeads * 8;               // one piece's (m, l): 128 B
+constexpr int kCombineStageWide = 20;                 // ... when there are few rows (one round for long rows)
+// query heads of one combine CTA when a row's merge is split over `parts` CTAs, and that
+// CTA's share of one piece: accumulators (head x 128 fp32) and (m, l) per head
+__host__ __device__ constexpr int combine_heads(int parts) { return kNumQHeads / parts; }
+__host__ __device__ constexpr int combine_acc_bytes(int parts) { return combine_heads(parts) * kHeadDim * 4; }
+__host__ __device__ constexpr int combine_ml_bytes(int parts) { return combine_heads(parts) * 8; }
 
 constexpr int kCombineRowsPerRound = 32;   // rows a CTA plans at once
 
 // Shared memory of a combine CTA staging `stage` pieces: this header, then the pieces'
-// accumulators (8 KiB each) and their (m, l) (128 B each).
+// accumulators and their (m, l) (this CTA's heads of them).
 struct CombineSmem {
     int4 job[kCombineRowsPerRound];   // {request, row, first piece, last piece} of the rows to merge
     int n_job;
     uint64_t full;
 };
 
-__host__ __device__ constexpr size_t combine_smem_bytes(int stage) {
-    return ((sizeof(CombineSmem) + 127) & ~size_t(127)) + (size_t)stage * (kCombineAccBytes + kCombineMlBytes) + 128;
+__host__ __device__ constexpr size_t combine_smem_bytes(int stage, int parts) {
+    return ((sizeof(CombineSmem) + 127) & ~size_t(127)) +
+           (size_t)stage * (combine_acc_bytes(parts) + combine_ml_bytes(parts)) + 128;
 }
 
 // Split-KV combine: every decode row whose blocks the decode kernel cut into several
 // pieces gets O = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p over its pieces
-// (M = max_p m_p), merged online piece by piece.  Two CTAs per row (16 query heads each,
-// one warp per head, lane l holding dims 4l .. 4l + 3); a CTA stages up to `stage`
+// (M = max_p m_p), merged online piece by piece.  kParts CTAs per row (32 / kParts query
+// heads each, one warp per head, lane l holding dims 4l .. 4l + 3); a CTA stages up to `stage`
 // pieces' partials at once in shared memory with bulk copies, so a row costs about one
 // round trip to memory.  Rows held by one piece were finished in place.  Launched after
 // the step's attention kernels, as a programmatic dependent: before its wait it works out
@@ -731,7 +733,8 @@ __host__ __device__ constexpr size_t combine_smem_bytes(int stage) {
 // let its dependents launch) and the decode launch's size; after the wait (for the decode
 // grid; the prefill grid, when there is one, completes only after it) only the copies and
 // the merge remain.
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const int32_t* __restrict__ page_off, int num_reqs,
+template <int kParts>
+__global__ void __launch_bounds__(kNumQHeads / kParts * 32) combine_kernel(const int32_t* __restrict__ page_off, int num_reqs,
                                                                    const int32_t* __restrict__ cu,
                                                                    const int32_t* __restrict__ counters,
                                                                    int decode_wave, int decode_grid,
@@ -742,20 +745,22 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const int32_t*
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     CombineSmem& S = *reinterpret_cast<CombineSmem*>(base);
-    float* s_acc = reinterpret_cast<float*>(base + ((sizeof(CombineSmem) + 127) & ~size_t(127)));   // [stage][16][128]
-    float2* s_ml = reinterpret_cast<float2*>(s_acc + (size_t)stage * kCombineHeads * kHeadDim);      // [stage][16]
-    const int half = blockIdx.x & 1;
+    constexpr int kCombineHeads = combine_heads(kParts);
+    constexpr int kCombineAccBytes = combine_acc_bytes(kParts), kCombineMlBytes = combine_ml_bytes(kParts);
+    float* s_acc = reinterpret_cast<float*>(base + ((sizeof(CombineSmem) + 127) & ~size_t(127)));   // [stage][heads][128]
+    float2* s_ml = reinterpret_cast<float2*>(s_acc + (size_t)stage * kCombineHeads * kHeadDim);      // [stage][heads]
+    const int part = (int)(blockIdx.x % kParts);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int head = half * kCombineHeads + warp;
+    const int head = part * kCombineHeads + warp;
     uint32_t phase = 0;
     if (threadIdx.x == 0) {
         mbar_init(&S.full, 1);
         fence_barrier_init();
     }
-    // This CTA pair takes rows blockIdx.x / 2 + k * stride; it plans up to
+    // This group of kParts CTAs takes rows blockIdx.x / kParts + k * stride; it plans up to
     // kCombineRowsPerRound of them at once (one thread each), then merges those to merge.
-    const int stride = gridDim.x >> 1;
-    for (int r0 = blockIdx.x >> 1; r0 < num_reqs; r0 += kCombineRowsPerRound * stride) {
+    const int stride = (int)(gridDim.x / kParts);
+    for (int r0 = (int)(blockIdx.x / kParts); r0 < num_reqs; r0 += kCombineRowsPerRound * stride) {
         if (threadIdx.x == 0) S.n_job = 0;
         __syncthreads();
         const int r = r0 + (int)threadIdx.x * stride;
@@ -790,9 +795,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const int32_t*
                     for (int j = 0; j < nb; ++j) {
                         const size_t slot = (size_t)job.x + b + j;
                         bulk_load(s_acc + (size_t)j * kCombineHeads * kHeadDim,
-                                  part_acc + (slot * kNumQHeads + half * kCombineHeads) * kHeadDim, kCombineAccBytes,
+                                  part_acc + (slot * kNumQHeads + part * kCombineHeads) * kHeadDim, kCombineAccBytes,
                                   &S.full, pol);
-                        bulk_load(s_ml + j * kCombineHeads, part_ml + slot * kNumQHeads + half * kCombineHeads,
+                        bulk_load(s_ml + j * kCombineHeads, part_ml + slot * kNumQHeads + part * kCombineHeads,
                                   kCombineMlBytes, &S.full,
                                   pol);
                     }
@@ -885,32 +890,42 @@ cudaError_t launch_decode(const StepArgs& a, const CUtensorMap* tmap_k, const CU
 cudaError_t launch_combine(const StepArgs& a, cudaStream_t stream) {
     const StepLayout& L = a.lay;
     const int wave = decode_wave(a);
-    // Two CTAs per row, and no more CTAs than run at once, each pair then taking several
-    // rows.  When there are at most as many rows as SM pairs, each CTA gets an SM to itself
-    // and stages 20 pieces at once (one round trip for the long rows of a mixed step);
-    // otherwise two CTAs per SM stage 12 each.  (Three CTAs per SM staging 8 pieces each
-    // merged the 256-row decode step more slowly: its longest rows took more rounds.)
+    // No more CTAs than run at once, each group then taking several rows.  With few rows
+    // (4 per row fit two to an SM) four CTAs of 8 heads share each row and stage 20 pieces
+    // at once, so the longest rows of a mixed step cost one round trip of ~80 KiB per SM;
+    // with at most as many rows as SM pairs, two CTAs of 16 heads per row, each with an SM
+    // to itself; otherwise two such CTAs per SM stage 12 pieces each.  (Three CTAs per SM
+    // staging 8 pieces each merged the 256-row decode step more slowly: its longest rows
+    // took more rounds.)
     const long long sms = a.num_sms > 0 ? a.num_sms : 1;
+    const bool quarter = 4LL * a.num_reqs <= 2 * sms;
     const bool wide = 2LL * a.num_reqs <= sms;
-    const int stage = wide ? kCombineStageWide : kCombineStage;
-    long long grid = 2LL * a.num_reqs;
-    const long long cap = wide ? sms / 2 * 2 : 2LL * sms;
+    const int parts = quarter ? 4 : 2;
+    const int stage = (quarter || wide) ? kCombineStageWide : kCombineStage;
+    long long grid = (long long)parts * a.num_reqs;
+    const long long cap = quarter ? 2 * sms / 4 * 4 : wide ? sms / 2 * 2 : 2LL * sms;
     if (grid > cap) grid = cap;
-    if (grid < 2) grid = 2;
-    return launch_pdl(combine_kernel, dim3((unsigned)grid), dim3(kCombineThreads), combine_smem_bytes(stage), stream,
-                      reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs, a.cu_seqlens_q,
-                      reinterpret_cast<const int32_t*>(a.ws + L.counters_off), wave, decode_grid(a, wave),
-                      reinterpret_cast<const float*>(a.ws + L.part_acc_off),
-                      reinterpret_cast<const float2*>(a.ws + L.part_ml_off), static_cast<__nv_bfloat16*>(a.out), a.err,
-                      stage);
+    if (grid < parts) grid = parts;
+    auto go = [&](auto kernel) {
+        return launch_pdl(kernel, dim3((unsigned)grid), dim3(kNumQHeads / parts * 32), combine_smem_bytes(stage, parts),
+                          stream, reinterpret_cast<const int32_t*>(a.ws + L.page_off_off), a.num_reqs, a.cu_seqlens_q,
+                          reinterpret_cast<const int32_t*>(a.ws + L.counters_off), wave, decode_grid(a, wave),
+                          reinterpret_cast<const float*>(a.ws + L.part_acc_off),
+                          reinterpret_cast<const float2*>(a.ws + L.part_ml_off), static_cast<__nv_bfloat16*>(a.out),
+                          a.err, stage);
+    };
+    return quarter ? go(combine_kernel<4>) : go(combine_kernel<2>);
 }
 
 cudaError_t configure_decode_kernel() {
     const cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)(sizeof(DecodeSmem) + 1024));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)combine_smem_bytes(kCombineStageWide));
+    const cudaError_t e2 = cudaFuncSetAttribute(combine_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)combine_smem_bytes(kCombineStageWide, 2));
+    if (e2 != cudaSuccess) return e2;
+    return cudaFuncSetAttribute(combine_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)combine_smem_bytes(kCombineStageWide, 4));
 }
 
 }  // namespace kvp
