@@ -17,16 +17,17 @@
 //   a few chunks that any CTA takes, through one global counter, once its own part is
 //   issued.  Fast SMs so take more chunks and all CTAs end together.
 // * Pieces (own parts and chunks) are numbered densely in sequence order.  A request cut
-//   by piece boundaries produces one partial per piece and KV head (slot r + piece); the
-//   last warp to finish a (request, KV head) merges them; a request inside one piece is
-//   finished in place.
+//   by piece boundaries produces one partial per piece (slot r + piece), which the
+//   combine kernel after the step's attention kernels merges; a request inside one piece
+//   is finished in place.
 // * One producer warp per CTA issues all copies: the block ids, requests and positions
 //   of the own part are looked up by the whole CTA up front (into shared memory), those
 //   of a chunk by a scheduler warp, which claims the chunk when the producer asks (a few
-//   blocks before it runs out of work) while earlier blocks stream.  One block of all 8 KV heads is 128 rows (head x token) of 128 dims in the
-//   pool, so its K and its V arrive with four tensor-map loads (one per 64-dim half,
-//   128-byte swizzle) into a 3-stage ring of 64 KiB stages; with each stage the producer
-//   hands the consumers the block's request, position and segment flags.
+//   blocks before it runs out of work) while earlier blocks stream.  One block of all 8
+//   KV heads is 128 rows (head x token) of 128 dims in the pool, so its K and its V
+//   arrive with four tensor-map loads (one per 64-dim half, 128-byte swizzle) into a
+//   3-stage ring of 64 KiB stages; with each stage the producer hands the consumers the
+//   block's request, position and segment flags.
 // * One consumer warp per KV head.  Its 4 query heads share every K/V byte (GQA
 //   packing), and the two contractions of a block are small matrix products, which run
 //   on the tensor cores (mma.sync m16n8k16, bf16 operands, fp32 accumulation) instead
@@ -724,10 +725,10 @@ __host__ __device__ constexpr size_t combine_smem_bytes(int stage, int parts) {
 
 // Split-KV combine: every decode row whose blocks the decode kernel cut into several
 // pieces gets O = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p over its pieces
-// (M = max_p m_p), merged online piece by piece.  kParts CTAs per row (32 / kParts query
-// heads each, one warp per head, lane l holding dims 4l .. 4l + 3); a CTA stages up to `stage`
-// pieces' partials at once in shared memory with bulk copies, so a row costs about one
-// round trip to memory.  Rows held by one piece were finished in place.  Launched after
+// (M = max_p m_p), merged online piece by piece.  kParts CTAs per row (32 / kParts
+// query heads each, one warp per head, lane l holding dims 4l .. 4l + 3); a CTA stages up
+// to `stage` pieces' partials at once in shared memory with bulk copies, so a row costs
+// about one round trip to memory.  Rows held by one piece were finished in place.  Launched after
 // the step's attention kernels, as a programmatic dependent: before its wait it works out
 // its row's pieces from the metadata kernel's outputs (complete before the decode kernel
 // let its dependents launch) and the decode launch's size; after the wait (for the decode
