@@ -129,22 +129,8 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-// Tiled tensor-map loads (the innermost coordinate must keep 16-byte alignment).
-__device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, int c0, int c1, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            smem_u32(smem_dst)),
-        "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// The same with shared-space addresses already converted (hot producer loops).
+// Tiled tensor-map loads (the innermost coordinate must keep 16-byte alignment); the 2-D
+// form takes shared-space addresses already converted (hot producer loops).
 __device__ __forceinline__ void tma_load_2d_u32(uint32_t smem_dst, const void* tmap, int c0, int c1, uint32_t bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -272,16 +258,6 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[12
         : "memory");
 }
 
-// 32 lanes x 16 consecutive 32-bit columns from registers (thread i -> lane i).
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
-}
-
 // Shared-memory matrix descriptor for tcgen05.mma (sm_100 family layout):
 // start address >> 4 in bits 0-13, leading-dimension byte offset >> 4 in bits 16-29,
 // stride-dimension byte offset >> 4 in bits 32-45, descriptor version 1 in bits 46-47,
@@ -309,9 +285,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_maj
 }
 
 // ------------------------------------------------------------------------ numerics
-
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Two floats to packed bf16x2 (round to nearest even); `lo` lands in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
