@@ -7,11 +7,15 @@ tcgen05 prefill tiles beside the split-KV decode, then the combine of split rows
 through the C ABI.
 
 Metric: packed query tokens/s per attention layer (T / step time), and the decode
-kernel's KV-read GB/s against the measured HBM peak.  Default workload: the mixed
-step (64 decode rows with context ~ U[128, 4096] plus two 512-token prefill chunks with
-0 and 1024 tokens cached, GQA 32/8, d 128, bf16, 32768-block pool).
+kernel's KV-read GB/s against the measured HBM peak.  Default workload: the largest
+single-GPU step, chunked prefill under an 8192-token budget (four 2048-token chunks
+after 0/2048/4096/6144 cached tokens plus 32 decode rows with context ~ U[512, 8192],
+GQA 32/8, d 128, bf16, 32768-block pool); its roofline is the prefill kernel's dense
+bf16 fraction.  The same JSON line carries the decode-heavy step (256 decode rows,
+lognormal contexts: the decode kernel's HBM fraction) and the mixed step (64 decode
+rows + two 512-token chunks), each timed the same way, under "workloads".
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config mixed|decode|chunked|tiny]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config chunked|mixed|decode|tiny|trace]
   python bench.py --impl reference ...   # the CPU oracle on the same workload
 
 Under torchrun (N > 1) every rank runs its own replica of the step on its own GPU (the
@@ -24,6 +28,7 @@ import argparse
 import hashlib
 import json
 import math
+import multiprocessing as mp
 import os
 import statistics
 import subprocess
@@ -35,7 +40,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-# The CPU oracle legs run on one core: keep BLAS single-threaded (set before numpy loads).
+# The CPU oracle runs one process per host core, each with BLAS on one thread (set
+# before numpy loads; spawned workers import this module again and inherit it).
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -166,117 +172,137 @@ def oracle_sample_rows(T, n_rows, shift=0):
     return np.unique(np.minimum(((np.arange(n) + frac) * (T / n)).astype(np.int64), T - 1))
 
 
-_ORACLE_INPUTS = {}
+_WORKER_INPUTS = {}
 
 
-def time_oracle(config, n_rows, min_seconds=0.0, shift=0):
-    """Wall time of the oracle (one process, BLAS limited to one thread at start-up) over
-    a sample of the step's rows, repeated until at least `min_seconds` have been timed.
-    Returns (rows computed, wall seconds, passes).  Input generation is outside the timed
-    calls."""
+def _oracle_inputs(config):
+    """The step's inputs from the seeded generator, drawn once per process."""
+    if config not in _WORKER_INPUTS:
+        from continuous_batching_paged_step_gb300 import workloads as wl
+        _WORKER_INPUTS[config] = wl.make_inputs(wl.CONFIGS[config]())
+    return _WORKER_INPUTS[config]
+
+
+def _oracle_worker_init(config):
+    _oracle_inputs(config)
+
+
+def _oracle_worker_ping(_):
+    time.sleep(0.05)
+    return os.getpid()
+
+
+def _oracle_worker_rows(args):
+    config, rows = args
     import oracle
-    from continuous_batching_paged_step_gb300 import workloads as wl
-    if config not in _ORACLE_INPUTS:
-        _ORACLE_INPUTS[config] = wl.make_inputs(wl.CONFIGS[config]())
-    inp = _ORACLE_INPUTS[config]
-    n, wall, passes = 0, 0.0, 0
-    while passes == 0 or wall < min_seconds:
-        rows = oracle_sample_rows(inp.spec.num_tokens, n_rows, shift + passes)
+    inp = _oracle_inputs(config)
+    out = oracle.step_reference(inp, rows=rows)
+    assert np.isfinite(out[rows]).all()
+    return len(rows)
+
+
+def oracle_tasks(cu_seqlens_q, context_lens, rows, n_tasks):
+    """Cut a sample of packed rows into about n_tasks lists, each holding rows of one
+    request of about equal oracle cost (a row scores its position + 1 keys), longest
+    first: the order a pool of workers takes them in."""
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    req = np.searchsorted(cu, rows, side="right") - 1
+    cost = ctx[req] + (rows - cu[req]) + 1
+    target = max(float(cost.sum()) / max(1, n_tasks), float(cost.max()))
+    tasks = []
+    for r in np.unique(req):
+        sel = req == r
+        cur, acc = [], 0.0
+        for x, c in zip(rows[sel], cost[sel]):
+            if cur and acc + c > target:
+                tasks.append((acc, cur))
+                cur, acc = [], 0.0
+            cur.append(int(x))
+            acc += float(c)
+        if cur:
+            tasks.append((acc, cur))
+    tasks.sort(key=lambda t: -t[0])
+    return [t[1] for t in tasks]
+
+
+class OracleTimer:
+    """The oracle as it stands, timed on the host's cores: `workers` processes (spawned,
+    so safe to start after CUDA is initialised), each with BLAS on one thread and its own
+    copy of the step's inputs drawn before any timing; a sample of rows is cut into
+    per-request tasks that the workers take longest first, and the wall time of the whole
+    sample is measured.  workers = 1 runs in this process."""
+
+    def __init__(self, config, workers=None):
+        from continuous_batching_paged_step_gb300 import workloads as wl
+        self.config = config
+        spec = wl.CONFIGS[config]()
+        self.cu = np.zeros(spec.num_reqs + 1, dtype=np.int64)
+        self.cu[1:] = np.cumsum(spec.q_lens)
+        self.ctx = np.asarray(spec.ctx_lens, dtype=np.int64)
+        self.workers = max(1, int(workers if workers else (os.cpu_count() or 1)))
+        self.pool = None
+        if self.workers > 1:
+            self.pool = mp.get_context("spawn").Pool(self.workers, initializer=_oracle_worker_init,
+                                                     initargs=(config,))
+            seen = set()
+            for _ in range(50):    # every worker has drawn its inputs once it answers
+                seen.update(self.pool.map(_oracle_worker_ping, range(4 * self.workers), chunksize=1))
+                if len(seen) >= self.workers:
+                    break
+        else:
+            _oracle_inputs(config)
+
+    def time_rows(self, rows):
+        """(rows computed, wall seconds) for one sample."""
+        if self.pool is None:
+            t0 = time.perf_counter()
+            n = _oracle_worker_rows((self.config, [int(x) for x in rows]))
+            return n, time.perf_counter() - t0
+        tasks = oracle_tasks(self.cu, self.ctx, rows, self.workers)
         t0 = time.perf_counter()
-        out = oracle.step_reference(inp, rows=rows)
-        wall += time.perf_counter() - t0
-        assert np.isfinite(out[rows]).all()
-        n += len(rows)
-        passes += 1
+        n = sum(self.pool.map(_oracle_worker_rows, [(self.config, t) for t in tasks], chunksize=1))
+        return n, time.perf_counter() - t0
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.close()
+            self.pool.join()
+            self.pool = None
+
+
+def time_oracle(config, n_rows, min_seconds=0.0, shift=0, timer=None):
+    """Wall time of the oracle over a sample of n_rows rows of the step, repeated (each
+    pass shifted) until at least `min_seconds` have been timed.  Returns (rows computed,
+    wall seconds, passes).  Input generation is outside the timed calls."""
+    own = timer is None
+    timer = timer or OracleTimer(config, workers=1)
+    from continuous_batching_paged_step_gb300 import workloads as wl
+    T = wl.CONFIGS[config]().num_tokens
+    n, wall, passes = 0, 0.0, 0
+    try:
+        while passes == 0 or wall < min_seconds:
+            rows = oracle_sample_rows(T, n_rows, shift + passes)
+            k, w = timer.time_rows(rows)
+            n += k
+            wall += w
+            passes += 1
+    finally:
+        if own:
+            timer.close()
     return n, wall, passes
 
 
 # ---------------------------------------------------------------------- GPU arm
 
-def run_gpu(a):
-    import torch
-    from continuous_batching_paged_step_gb300 import build as b
-    b.build()
-    from continuous_batching_paged_step_gb300 import kvpaged as kp
-    from continuous_batching_paged_step_gb300 import runner, workloads as wl
+SIDE_WORKLOADS = ("decode", "mixed", "chunked")
 
-    from continuous_batching_paged_step_gb300 import replicas
-    rank, world, local = replicas.dist_env()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    dist = replicas.init("nccl", device=dev)
 
-    spec = wl.CONFIGS[a.config]()
-    inp = wl.make_inputs(spec)
-    step = runner.PagedStep(inp, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    T = spec.num_tokens
+def rooflines(spec, kern):
+    """(dominant kernel's roofline, the other attention kernel's) for one workload."""
+    hbm, bf16, _, peak_src = peaks()
     work = work_of(spec)
-
-    def barrier():
-        replicas.barrier(dist)
-
-    # warm-up
-    for i in range(a.warmup):
-        flush.fill_(i & 0xFF)
-        step.run()
-    torch.cuda.synchronize(dev)
-    st = step.error()
-    if st != (0, 0):
-        raise RuntimeError(f"device error word after warm-up: {st}")
-
-    clocks = ClockSampler(dev.index if dev.index is not None else 0)
-    clocks.start()
-    time.sleep(0.25)
-
-    def timed_steps(n):
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        barrier()
-        torch.cuda.synchronize(dev)
-        for i in range(n):
-            flush.fill_((i + 1) & 0xFF)        # L2 flush between steps, outside the step's events
-            starts[i].record(stream)
-            step.run()
-            ends[i].record(stream)
-        torch.cuda.synchronize(dev)
-        barrier()
-        return [s.elapsed_time(e) for s, e in zip(starts, ends)]
-
-    # headline: the steps as a user runs them (no timing events inside the library calls)
-    launches0 = kp.kv_pool_launch_count(step.pool.handle)
-    wall0 = time.perf_counter()
-    step_ms = timed_steps(a.steps)
-    wall = time.perf_counter() - wall0
-    launches = kp.kv_pool_launch_count(step.pool.handle) - launches0
-    # the same number of steps again with CUDA events around every kernel the library
-    # launches, on its launch stream: per-kernel durations for the roofline
-    kp.kv_pool_enable_timing(step.pool.handle, 8 * a.steps + 16)
-    step_ms_kernels = timed_steps(a.steps)
-    per_kernel = kp.kv_pool_read_timing(step.pool.handle)
-    kp.kv_pool_enable_timing(step.pool.handle, 0)
-    clk = clocks.stop()
-    st = step.error()
-    if st != (0, 0):
-        raise RuntimeError(f"device error word after the timed steps: {st}")
-    total_ms = replicas.max_over_ranks(dist, sum(step_ms), device=dev)
-    value = replicas.aggregate_rate(T * a.steps, world, total_ms)
-
-    # ----------------------------------------------------------- end to end (host buffers)
-    e2e = run_e2e(a, step, stream, dev, flush, dist, world)
-
-    if rank != 0:
-        step.close()
-        if dist is not None:
-            dist.destroy_process_group()
-        return None
-
-    hbm, bf16, bf16_sus, peak_src = peaks()
-    kern = {}
-    for name, (n, ms) in per_kernel.items():
-        if n:
-            kern[name] = {"launches": n, "avg_us": 1e3 * ms / n}
     dec_us = kern.get("decode_splitkv", {}).get("avg_us")
     pre_us = kern.get("prefill_tcgen05", {}).get("avg_us")
     dominant = max(kern, key=lambda k: kern[k]["avg_us"] * kern[k]["launches"]) if kern else None
@@ -286,49 +312,181 @@ def run_gpu(a):
         rl_decode = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(ach / hbm, 4), "traffic": ncu_traffic("decode_splitkv", spec.name),
                      "kernel": "decode_splitkv", "algorithmic_bytes_per_launch": work["decode_bytes"],
-                     "peak_source": f"hbm_gbs, {peak_src}"}
+                     "avg_us": round(dec_us, 2), "peak_source": f"hbm_gbs, {peak_src}"}
     rl_prefill = None
     if pre_us and work["prefill_flops"]:
         ach = work["prefill_flops"] / (pre_us * 1e-6) / 1e12
         rl_prefill = {"bound": "tensor", "achieved": round(ach, 1), "peak": bf16, "unit": "TFLOP/s",
                       "frac": round(ach / bf16, 4), "traffic": ncu_traffic("prefill_tcgen05", spec.name),
                       "kernel": "prefill_tcgen05", "algorithmic_flops_per_launch": work["prefill_flops"],
-                      "peak_source": f"bf16_tflops (burst), {peak_src}"}
+                      "avg_us": round(pre_us, 2), "peak_source": f"bf16_tflops (burst), {peak_src}"}
     roofline = rl_prefill if dominant == "prefill_tcgen05" else rl_decode
     secondary = rl_decode if roofline is rl_prefill else rl_prefill
+    return roofline, secondary
+
+
+def measure_step(spec, a, dev, dist, world, flush, with_e2e):
+    """One workload on this GPU: W warm-up steps, K timed steps (CUDA events on the
+    launching stream, L2 flushed between steps outside the events), K more steps with the
+    library's events around each of its kernels (per-kernel durations), and optionally
+    the end-to-end leg.  Returns the measurements; closes the step."""
+    import torch
+    from continuous_batching_paged_step_gb300 import kvpaged as kp
+    from continuous_batching_paged_step_gb300 import replicas, runner, workloads as wl
+    inp = wl.make_inputs(spec)
+    step = runner.PagedStep(inp, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    try:
+        for i in range(a.warmup):
+            flush.fill_(i & 0xFF)
+            step.run()
+        torch.cuda.synchronize(dev)
+        st = step.error()
+        if st != (0, 0):
+            raise RuntimeError(f"{spec.name}: device error word after warm-up: {st}")
+
+        def timed_steps(n):
+            starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+            ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+            replicas.barrier(dist)
+            torch.cuda.synchronize(dev)
+            for i in range(n):
+                flush.fill_((i + 1) & 0xFF)        # L2 flush between steps, outside the step's events
+                starts[i].record(stream)
+                step.run()
+                ends[i].record(stream)
+            torch.cuda.synchronize(dev)
+            replicas.barrier(dist)
+            return [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
+
+        # the steps as a user runs them (no timing events inside the library calls)
+        launches0 = kp.kv_pool_launch_count(step.pool.handle)
+        wall0 = time.perf_counter()
+        step_ms = timed_steps(a.steps)
+        wall = time.perf_counter() - wall0
+        launches = kp.kv_pool_launch_count(step.pool.handle) - launches0
+        # the same number of steps with CUDA events around every kernel the library
+        # launches, on its launch stream: per-kernel durations for the roofline
+        kp.kv_pool_enable_timing(step.pool.handle, 8 * a.steps + 16)
+        step_ms_kernels = timed_steps(a.steps)
+        per_kernel = kp.kv_pool_read_timing(step.pool.handle)
+        kp.kv_pool_enable_timing(step.pool.handle, 0)
+        st = step.error()
+        if st != (0, 0):
+            raise RuntimeError(f"{spec.name}: device error word after the timed steps: {st}")
+        total_ms = replicas.max_over_ranks(dist, sum(step_ms), device=dev)
+        e2e = run_e2e(a, step, stream, dev, dist, world, total_ms / a.steps) if with_e2e else None
+    finally:
+        step.close()
+    kern = {name: {"launches": n, "avg_us": 1e3 * ms / n} for name, (n, ms) in per_kernel.items() if n}
+    T = spec.num_tokens
+    return {"value": replicas.aggregate_rate(T * a.steps, world, total_ms), "total_ms": total_ms,
+            "ms_per_step_with_kernel_events": sum(step_ms_kernels) / a.steps, "kern": kern,
+            "launches": int(launches), "wall": wall, "e2e": e2e}
+
+
+def run_gpu(a):
+    import torch
+    from continuous_batching_paged_step_gb300 import build as b
+    b.build()
+    from continuous_batching_paged_step_gb300 import replicas, workloads as wl
+    rank, world, local = replicas.dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = replicas.init("nccl", device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    spec = wl.CONFIGS[a.config]()
+    sides = [] if (a.no_side_workloads or a.config not in SIDE_WORKLOADS) else \
+        [c for c in SIDE_WORKLOADS if c != a.config]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.25)
+    main = measure_step(spec, a, dev, dist, world, flush, with_e2e=True)
+    side = {}
+    for c in sides:
+        sp = wl.CONFIGS[c]()
+        side[sp.name] = (sp, measure_step(sp, a, dev, dist, world, flush, with_e2e=False))
+    clk = clocks.stop()
+    del flush
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    roofline, secondary = rooflines(spec, main["kern"])
+    workloads = {}
+    for name, (sp, m) in side.items():
+        rl, rl2 = rooflines(sp, m["kern"])
+        workloads[name] = {"value": round(m["value"], 1), "unit": UNIT, "steps": a.steps,
+                           "ms_per_step": round(m["total_ms"] / a.steps, 5), "num_tokens": sp.num_tokens,
+                           "roofline": rl, "roofline_secondary": rl2,
+                           "kernels_us": {k: round(v["avg_us"], 2) for k, v in m["kern"].items()},
+                           "gpu_launches": m["launches"]}
+
+    def frac_of(rl_pair, kernel):
+        for rl in rl_pair:
+            if rl and rl["kernel"] == kernel:
+                return rl["frac"]
+        return None
+
+    targets = {"prefill_tensor_frac": frac_of((roofline, secondary), "prefill_tcgen05"),
+               "prefill_tensor_frac_workload": spec.name}
+    dh = wl.CONFIGS["decode"]().name
+    if dh == spec.name:
+        targets["decode_heavy_hbm_frac"] = frac_of((roofline, secondary), "decode_splitkv")
+    elif dh in workloads:
+        targets["decode_heavy_hbm_frac"] = frac_of((workloads[dh]["roofline"], workloads[dh]["roofline_secondary"]),
+                                                   "decode_splitkv")
+    targets["targets"] = "decode-dominated steps >= 0.70 of HBM peak; prefill tiles >= 0.50 of dense bf16 peak"
 
     cpu = None
     if not a.no_cpu_baseline:
-        # a short probe sizes the sample: as many evenly spaced rows as one pass of about
-        # oracle_seconds allows (the whole step when it fits), repeated up to that time
-        n_probe, w_probe, _ = time_oracle(a.config, 32)
-        n_pass = min(T, max(32, int(n_probe / max(w_probe, 1e-6) * a.oracle_seconds)))
-        n_rows, owall, passes = time_oracle(a.config, n_pass, a.oracle_seconds)
-        cpu = {"value": round(n_rows / owall, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{passes} pass(es) over {n_rows // passes} of {T} packed rows of the {spec.name} step, "
-                         f"evenly spaced over the step (decode and prefill rows in proportion), fp64 numpy, "
-                         f"one process, {owall:.1f} s"}
+        cpu = cpu_baseline(a, spec)
 
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": a.steps,
-        "warmup": a.warmup, "ms_per_step": round(total_ms / a.steps, 5), "higher_is_better": True,
+        "metric": METRIC, "value": round(main["value"], 1), "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": round(main["total_ms"] / a.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": step_config(spec, world),
-        "decode_kv_gbs": rl_decode["achieved"] if rl_decode else None,
-        "roofline": roofline, "roofline_secondary": secondary,
-        "kernels_us": {k: round(v["avg_us"], 2) for k, v in kern.items()},
-        "ms_per_step_with_kernel_events": round(sum(step_ms_kernels) / a.steps, 5),
-        "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": int(launches),
-        "wall_s_timed": round(wall, 3),
+        "decode_kv_gbs": next((rl["achieved"] for rl in (roofline, secondary) if rl and rl["kernel"] == "decode_splitkv"),
+                              None),
+        "roofline": roofline, "roofline_secondary": secondary, **targets,
+        "kernels_us": {k: round(v["avg_us"], 2) for k, v in main["kern"].items()},
+        "ms_per_step_with_kernel_events": round(main["ms_per_step_with_kernel_events"], 5),
+        "workloads": workloads,
+        "cpu_baseline": cpu, "e2e": main["e2e"], "clocks": clk, "gpu_launches": main["launches"],
+        "wall_s_timed": round(main["wall"], 3),
     }
     print(json.dumps(line), flush=True)
-    step.close()
     if dist is not None:
         dist.destroy_process_group()
     return line
 
 
-def run_e2e(a, step, stream, dev, flush, dist, world):
+def cpu_baseline(a, spec):
+    """The oracle on the host's cores, on a bounded sample of the workload: a short probe
+    sizes one pass (as many evenly spaced rows as about --oracle-seconds allow, the whole
+    step when it fits), repeated until that much oracle time is measured."""
+    timer = OracleTimer(a.config, workers=a.oracle_workers or None)
+    try:
+        T = spec.num_tokens
+        n_probe, w_probe, _ = time_oracle(a.config, 4 * timer.workers, timer=timer)
+        n_pass = min(T, max(4 * timer.workers, int(n_probe / max(w_probe, 1e-6) * a.oracle_seconds)))
+        n_rows, owall, passes = time_oracle(a.config, n_pass, a.oracle_seconds, timer=timer)
+    finally:
+        timer.close()
+    return {"value": round(n_rows / owall, 3), "unit": UNIT, "cores": timer.workers, "kind": "oracle",
+            "sample": f"{passes} pass(es) over {n_rows // passes} of {T} packed rows of the {spec.name} step, "
+                      f"evenly spaced over the step (decode and prefill rows in proportion), fp64 numpy, "
+                      f"{timer.workers} processes with one BLAS thread each, {owall:.1f} s"}
+
+
+E2E_MIN_MS = 200.0
+E2E_MAX_STEPS = 5000
+
+
+def run_e2e(a, step, stream, dev, dist, world, est_ms):
     """Same metric through the C ABI with host buffers, as a serving loop runs it: every
     step's inputs go host -> device from pinned memory and its output device -> host,
     inside the timed region.  The copies are pipelined with the compute: two sets of
@@ -336,7 +494,9 @@ def run_e2e(a, step, stream, dev, flush, dist, world):
     upload and step i-1's download overlap step i's kernels (and each other: an upload
     waits only for the step that last read its input set, a step only for the download of
     the output set it overwrites).  No L2 flush here: every step streams the decode rows'
-    whole KV history (hundreds of MB, more than L2)."""
+    whole KV history (hundreds of MB, more than L2).  At least --steps steps are timed, and
+    enough that the timed region lasts about E2E_MIN_MS (the pipeline's fill and drain are
+    then a small part of it); the count is reported."""
     import torch
     from continuous_batching_paged_step_gb300 import kvpaged as kp
     from continuous_batching_paged_step_gb300 import replicas
@@ -368,7 +528,7 @@ def run_e2e(a, step, stream, dev, flush, dist, world):
     h2d = total_bytes
     d2h = out_h[0].numel() * out_h[0].element_size()
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    n = max(4, a.steps // 4)
+    n = int(min(E2E_MAX_STEPS, max(a.steps, math.ceil(E2E_MIN_MS / max(est_ms, 1e-3)))))
     # events reused by parity: step i waits on those step i - 2 recorded, before it records its own
     loaded = torch.cuda.Event()
     computed = [torch.cuda.Event() for _ in range(2)]   # step's kernels finished (its input set is free)
@@ -427,35 +587,39 @@ def step_config(spec, world):
 
 
 def run_reference(a):
-    """The CPU oracle as it stands, on the same workload: each step is the oracle over a
-    bounded sample of the step's rows, sized so the whole run takes a few minutes."""
+    """The CPU oracle as it stands, on the same workload, on the host's cores: each step is
+    the oracle over a bounded sample of the step's rows, sized so the whole run takes a
+    few minutes."""
     if int(os.environ.get("RANK", "0")) != 0:
         return None
     from continuous_batching_paged_step_gb300 import workloads as wl
     spec = wl.CONFIGS[a.config]()
-    workers = 1
+    timer = OracleTimer(a.config, workers=a.oracle_workers or None)
     budget_s = 150.0
-    # first timed probe with a small sample, then size the per-step sample to the budget
-    # (at least 16 evenly spaced rows a step)
-    n_probe, w, _ = time_oracle(a.config, 32)
-    per_step_target = budget_s / max(1, a.steps + a.warmup)
-    n_pass = min(spec.num_tokens, max(8, int(n_probe / max(w, 1e-6) * per_step_target)))
-    rows_timed, t_timed = 0, 0.0
-    for i in range(a.warmup + a.steps):
-        n_rows, w, _ = time_oracle(a.config, n_pass, shift=i)
-        if i >= a.warmup:
-            rows_timed += n_rows
-            t_timed += w
+    try:
+        # a timed probe with a small sample sizes the per-step sample to the budget (at
+        # least 8 evenly spaced rows a step)
+        n_probe, w, _ = time_oracle(a.config, 4 * timer.workers, timer=timer)
+        per_step_target = budget_s / max(1, a.steps + a.warmup)
+        n_pass = min(spec.num_tokens, max(8, int(n_probe / max(w, 1e-6) * per_step_target)))
+        rows_timed, t_timed = 0, 0.0
+        for i in range(a.warmup + a.steps):
+            n_rows, w, _ = time_oracle(a.config, n_pass, shift=i, timer=timer)
+            if i >= a.warmup:
+                rows_timed += n_rows
+                t_timed += w
+    finally:
+        timer.close()
     per = t_timed / max(1, a.steps)
     value = rows_timed / max(t_timed, 1e-9)
     sample = (f"{n_pass} of {spec.num_tokens} packed rows per step of the {spec.name} step, evenly spaced over "
-              f"the step (decode and prefill rows in proportion, shifted from step to step); value = rows / time "
-              f"over the timed steps")
+              f"the step (decode and prefill rows in proportion, shifted from step to step), {timer.workers} "
+              f"processes with one BLAS thread each; value = rows / time over the timed steps")
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(per * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": step_config(spec, int(os.environ.get("WORLD_SIZE", "1"))),
-            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": workers, "kind": "oracle",
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": timer.workers, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -521,10 +685,15 @@ def main():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", choices=["mixed", "decode", "chunked", "tiny", "trace"], default="mixed")
+    p.add_argument("--config", choices=["chunked", "mixed", "decode", "tiny", "trace"], default="chunked")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-side-workloads", action="store_true",
+                   help="time only --config (by default the chunked, mixed and decode-heavy steps are all timed "
+                        "and the others reported under 'workloads')")
     p.add_argument("--oracle-seconds", type=float, default=10.0,
                    help="the cpu_baseline repeats its sample until this much oracle time is measured")
+    p.add_argument("--oracle-workers", type=int, default=0,
+                   help="oracle processes for the CPU legs (0: one per host core)")
     a = p.parse_args()
     if a.warmup < 3:
         p.error("--warmup must be at least 3")

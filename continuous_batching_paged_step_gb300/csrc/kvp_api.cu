@@ -3,6 +3,7 @@
 // paged_attention_step.  Host code only; kernels live in the other .cu files.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cstring>
@@ -41,6 +42,7 @@ struct kvp_pool {
     CUtensorMap tmap_k_blk;   // whole blocks: boxes of 128 rows (decode)
     CUtensorMap tmap_v_blk;
     // diagnostics
+    int nvtx = 0;   // NVTX ranges around the library's calls and launches (off by default)
     long long launches = 0;
     std::vector<cudaEvent_t> t_events;  // 2 per timed launch
     std::vector<int> t_kind;
@@ -178,10 +180,51 @@ kvp_status upload_refcounts(kvp_pool* p, cudaStream_t stream) {
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+// An NVTX range in the library's own domain ("kvpaged") for the lifetime of the object,
+// when the pool has ranges switched on: a profiler's timeline then shows kv_append, the
+// attention step and each kernel launch by name.  Without a profiler attached the NVTX
+// calls do nothing.
+class NvtxRange {
+   public:
+    NvtxRange(const kvp_pool* p, const char* name) : on_(p && p->nvtx) {
+        if (!on_) return;
+        static nvtxDomainHandle_t dom = nvtxDomainCreateA("kvpaged");
+        dom_ = dom;
+        nvtxEventAttributes_t ev = {};
+        ev.version = NVTX_VERSION;
+        ev.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+        ev.messageType = NVTX_MESSAGE_TYPE_ASCII;
+        ev.message.ascii = name;
+        nvtxDomainRangePushEx(dom_, &ev);
+    }
+    ~NvtxRange() {
+        if (on_) nvtxDomainRangePop(dom_);
+    }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+
+   private:
+    bool on_;
+    nvtxDomainHandle_t dom_ = nullptr;
+};
+
+const char* kernel_name(int kind) {
+    switch (kind) {
+        case KVP_KERNEL_APPEND: return "kv_append_kernel";
+        case KVP_KERNEL_PREP: return "step_prep_kernel";
+        case KVP_KERNEL_PREFILL: return "prefill_kernel";
+        case KVP_KERNEL_DECODE: return "decode_kernel";
+        case KVP_KERNEL_BLOCKS: return "block_move_kernel";
+        case KVP_KERNEL_COMBINE: return "combine_kernel";
+    }
+    return "kernel";
+}
+
 // Launch one kernel through `fn`, counting it and, when timing is on, bracketing it with
 // the next pair of events.
 template <class F>
 cudaError_t timed_launch(kvp_pool* p, int kind, cudaStream_t s, F&& fn) {
+    NvtxRange range(p, kernel_name(kind));
     const int slot = p->t_used;
     const bool timed = slot < (int)p->t_kind.size();
     if (timed && cudaEventRecord(p->t_events[2 * slot], s) != cudaSuccess) return cudaErrorUnknown;
@@ -427,6 +470,12 @@ int kv_block_refcount(const kvp_pool* p, int32_t id) {
     return p->refcnt[id];
 }
 
+kvp_status kv_pool_set_nvtx(kvp_pool* p, int on) {
+    if (!p) return KVP_E_INVALID_ARG;
+    p->nvtx = on ? 1 : 0;
+    return KVP_OK;
+}
+
 kvp_status kv_pool_set_decode_ctas(kvp_pool* p, int ctas) {
     if (!p || ctas < 0 || ctas > kvp::kMaxDecodeCtas) return KVP_E_INVALID_ARG;
     p->decode_ctas = ctas;
@@ -441,6 +490,7 @@ kvp_status kv_append(kvp_pool* p, const void* k_new, const void* v_new, const in
     if (num_reqs < 1 || max_blocks_per_seq < 1 || !k_new || !v_new || !cu_seqlens_q || !context_lens ||
         !block_tables || !aligned16(k_new) || !aligned16(v_new))
         return KVP_E_INVALID_ARG;
+    NvtxRange range(p, "kv_append");
     kvp_status st = ensure_device(p);
     if (st != KVP_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -472,6 +522,7 @@ kvp_status paged_attention_step(kvp_pool* p, const void* q, void* out, const int
     kvp::StepLayout lay = kvp::make_step_layout(num_reqs, num_tokens);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < lay.total)
         return KVP_E_WORKSPACE;
+    NvtxRange range(p, "paged_attention_step");
     kvp_status st = ensure_device(p);
     if (st != KVP_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -37,6 +37,7 @@ SIGNATURES = {
     "paged_attention_workspace_size": (_SZ, [_P, _I, _I, _I, _I]),
     "paged_attention_step": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
     "kv_pool_set_decode_ctas": (_I, [_P, _I]),
+    "kv_pool_set_nvtx": (_I, [_P, _I]),
     "kv_pool_get_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
     "kvp_status_string": (ctypes.c_char_p, [_I]),
     "kv_pool_enable_timing": (_I, [_P, _I]),
@@ -207,6 +208,11 @@ def kv_block_refcount(pool: int, block_id: int) -> int:
 def kv_pool_set_decode_ctas(pool: int, ctas: int):
     """Number of CTAs the decode blocks are shared out among (0 = one per SM)."""
     _check(lib.kv_pool_set_decode_ctas(pool, ctas), "kv_pool_set_decode_ctas")
+
+
+def kv_pool_set_nvtx(pool: int, on: bool):
+    """NVTX ranges (domain "kvpaged") around this pool's calls and kernel launches."""
+    _check(lib.kv_pool_set_nvtx(pool, 1 if on else 0), "kv_pool_set_nvtx")
 
 
 def kv_pool_get_error(pool: int, stream=None):

@@ -263,3 +263,146 @@ def trace_rows(seed: int, rid: int, start: int, n: int, n_q: int = N_Q_HEADS * H
     return (_normal_bf16(seed, rid + 1, _TRACE_Q * 100003 + start, (n, n_q)),
             _normal_bf16(seed, rid + 1, _TRACE_K * 100003 + start, (n, n_kv)),
             _normal_bf16(seed, rid + 1, _TRACE_V * 100003 + start, (n, n_kv)))
+
+
+# --------------------------------------------------------------------------------------
+# Shaped inputs for sensitive parity checks.  With N(0, 1) queries and keys the scores
+# are ~N(0, 1), attention is close to uniform over a long history, and one 16-key block
+# more or less moves a row's output by less than the comparison tolerance.  These
+# shapers move input values only (no attention arithmetic): they add a per-(request,
+# KV group) direction d to the query rows and place keys along it, so that chosen keys
+# dominate every row's weights ("needles") or so that scores climb along the history
+# (the running maximum keeps moving until the last keys).
+# --------------------------------------------------------------------------------------
+
+def long_context_step(seed: int = 0xC0FFEE + 21) -> StepSpec:
+    """Decode rows over contexts from 0 to 8192 (block-boundary values included) and
+    prefill chunks after long cached prefixes: 2048 rows after 6144, 300 after 4000, 130
+    after nothing and 33 after 127 (a chunk that starts one key before a 128-key tile)."""
+    rng = np.random.default_rng([seed, 1])
+    dec = [8192, 8191, 8177, 8176, 6000, 4096, 4095, 3333, 2048, 1024, 1023, 767, 512, 511, 300, 257, 256,
+           255, 100, 31, 16, 15, 1, 0]
+    dec += rng.integers(1, 8192, size=8, endpoint=True).tolist()
+    chunks = [(2048, 6144), (300, 4000), (130, 0), (33, 127)]
+    q_lens = [1] * len(dec) + [c[0] for c in chunks]
+    ctx = dec + [c[1] for c in chunks]
+    # interleave the chunks among the decode rows so request order is mixed
+    order = np.random.default_rng([seed, 2]).permutation(len(q_lens)).tolist()
+    q_lens = [q_lens[i] for i in order]
+    ctx = [ctx[i] for i in order]
+    need = sum(-(-(c + q) // BLOCK_SIZE) for c, q in zip(ctx, q_lens))
+    return StepSpec("long-context", q_lens=q_lens, ctx_lens=ctx, num_blocks=need + 97, seed=seed)
+
+
+def _as_f32(bits):
+    return bf16_bits_to_f32(bits).copy()
+
+
+def _key_row(inp: StepInputs, r: int, t: int, which: str):
+    """(array, row index) holding position t of request r's K (which='k') or V history."""
+    ctx = int(inp.context_lens[r])
+    if t < ctx:
+        return (inp.k_prior if which == "k" else inp.v_prior)[r], t
+    return (inp.k_new if which == "k" else inp.v_new), int(inp.cu_seqlens_q[r]) + t - ctx
+
+
+def _copy_inputs(inp: StepInputs) -> StepInputs:
+    return StepInputs(spec=inp.spec, q=inp.q.copy(), k_new=inp.k_new.copy(), v_new=inp.v_new.copy(),
+                      k_prior=[None if a is None else a.copy() for a in inp.k_prior],
+                      v_prior=[None if a is None else a.copy() for a in inp.v_prior],
+                      cu_seqlens_q=inp.cu_seqlens_q, context_lens=inp.context_lens,
+                      block_tables=inp.block_tables, block_order=inp.block_order)
+
+
+def _directions(spec: StepSpec, seed: int):
+    """A unit-variance direction per (request, KV group): float32 [R, n_kv, d]."""
+    rng = np.random.default_rng([seed, 0xD1])
+    return rng.standard_normal((spec.num_reqs, spec.n_kv_heads, spec.head_dim)).astype(np.float32)
+
+
+def _add_to_queries(out: StepInputs, d, beta: float):
+    """Query rows of request r, every head of KV group g: q += beta * d[r, g]."""
+    spec = out.spec
+    g = spec.n_q_heads // spec.n_kv_heads
+    q = _as_f32(out.q).reshape(-1, spec.n_kv_heads, g, spec.head_dim)
+    cu = out.cu_seqlens_q
+    for r in range(spec.num_reqs):
+        s, e = int(cu[r]), int(cu[r + 1])
+        if e > s:
+            q[s:e] += beta * d[r][None, :, None, :]
+    out.q = f32_to_bf16_bits(q.reshape(out.q.shape))
+
+
+def needle_positions(spec: StepSpec, every_block_max: int = 48, spread: int = 16):
+    """Key positions planted as needles, per request.  A history of at most
+    `every_block_max` blocks gets one needle in every block (offsets inside the block
+    cycle through 0, 15, 7, 8, 3, 12, ...); a longer one gets `spread` needles in blocks
+    spread evenly from its first to its last block, offsets alternating 0 and 15."""
+    offs = [0, 15, 7, 8, 3, 12, 1, 14, 5, 10]
+    out = []
+    for r in range(spec.num_reqs):
+        n = spec.ctx_lens[r] + spec.q_lens[r]
+        if spec.q_lens[r] == 0 or n == 0:
+            out.append([])
+            continue
+        nb = -(-n // spec.block_size)
+        if nb <= every_block_max:
+            blocks = list(range(nb))
+        else:
+            blocks = sorted(set(int(round(k * (nb - 1) / (spread - 1))) for k in range(spread)))
+        pos = []
+        for i, b in enumerate(blocks):
+            o = offs[i % len(offs)] if nb <= every_block_max else (0 if i % 2 == 0 else 15)
+            pos.append(min(b * spec.block_size + o, n - 1))
+        out.append(sorted(set(pos)))
+    return out
+
+
+def plant_needles(inp: StepInputs, alpha: float = 0.5, beta: float = 4.0, v_scale: float = 0.5,
+                  seed: int = 0xBEEF, positions=None):
+    """Needle inputs: query rows of request r get beta * d[r, g] added on every head of
+    KV group g; the key at each needle position becomes alpha * d[r, g] (so its score,
+    about alpha * beta * d . d / sqrt(d), is far above the other keys' for every row that
+    sees it) and its value is scaled by v_scale (keeps outputs near the values' scale).
+    Returns (inputs, positions)."""
+    spec = inp.spec
+    out = _copy_inputs(inp)
+    d = _directions(spec, seed)
+    _add_to_queries(out, d, beta)
+    pos = needle_positions(spec) if positions is None else positions
+    for r, ps in enumerate(pos):
+        for t in ps:
+            ka, ki = _key_row(out, r, t, "k")
+            ka[ki] = f32_to_bf16_bits((alpha * d[r]).reshape(-1))
+            va, vi = _key_row(out, r, t, "v")
+            va[vi] = f32_to_bf16_bits(_as_f32(va[vi]) * np.float32(v_scale))
+    return out, pos
+
+
+def plant_late_peak(inp: StepInputs, gamma_max: float = 5.0, beta: float = 1.0, v_scale: float = 0.5,
+                    seed: int = 0xFEED):
+    """Late-peak inputs: query rows of request r get beta * d[r, g] added; the key at
+    position t of a history of n keys gets gamma_max * t / (n - 1) * d[r, g] added, so
+    scores climb by tens of units along the history and the running maximum keeps
+    moving until the last keys.  Values are scaled by v_scale."""
+    spec = inp.spec
+    out = _copy_inputs(inp)
+    d = _directions(spec, seed)
+    _add_to_queries(out, d, beta)
+    kn = _as_f32(out.k_new).reshape(-1, spec.n_kv_heads, spec.head_dim)
+    cu = out.cu_seqlens_q
+    for r in range(spec.num_reqs):
+        c, ql = spec.ctx_lens[r], spec.q_lens[r]
+        n = c + ql
+        if ql == 0 or n < 2:
+            continue
+        ramp = (gamma_max * np.arange(n, dtype=np.float32) / np.float32(n - 1))[:, None, None] * d[r][None]
+        if c > 0:
+            kp = _as_f32(out.k_prior[r]).reshape(c, spec.n_kv_heads, spec.head_dim) + ramp[:c]
+            out.k_prior[r] = f32_to_bf16_bits(kp.reshape(c, -1))
+            out.v_prior[r] = f32_to_bf16_bits(_as_f32(out.v_prior[r]) * np.float32(v_scale))
+        s = int(cu[r])
+        kn[s:s + ql] += ramp[c:]
+    out.k_new = f32_to_bf16_bits(kn.reshape(out.k_new.shape))
+    out.v_new = f32_to_bf16_bits(_as_f32(out.v_new) * np.float32(v_scale))
+    return out

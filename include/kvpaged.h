@@ -251,7 +251,9 @@ KVP_API kvp_status kv_pool_get_error(kvp_pool* pool, kvp_stream stream, uint32_t
  * its KV pool, or a serving loop that must not call cudaMalloc/cudaFree because they can
  * synchronise the device).  The scratch lives in a fixed device array inside the library
  * (paged_attention_noalloc_capacity() bytes, 32 MiB), held by every GPU that loads the
- * library until the process exits.  The call allocates nothing: the pool must already
+ * library until the process exits.  It holds the scratch of a step of at most about 990
+ * requests (991 for a decode-only step): every request and each of the decode kernel's up
+ * to 1,024 pieces has a slot of split-KV partials of about 16.6 KiB.  The call allocates nothing: the pool must already
  * have its device state (made by its first kv_append on the current device), else
  * KVP_E_INVALID_ARG.  A step whose scratch (paged_attention_workspace_size) exceeds the
  * array is rejected with KVP_E_WORKSPACE before anything is launched.  All calls share
@@ -288,6 +290,14 @@ KVP_API size_t paged_attention_noalloc_capacity(void);
 #define KVP_NUM_KERNELS    6
 KVP_API kvp_status kv_pool_enable_timing(kvp_pool* pool, int max_launches);
 KVP_API kvp_status kv_pool_read_timing(kvp_pool* pool, int* counts, float* ms);
+
+/* NVTX ranges (domain "kvpaged"): with on != 0, kv_append, paged_attention_step, the
+ * block copies and every kernel launch of this pool are wrapped in named ranges
+ * (kv_append, paged_attention_step, kv_append_kernel, step_prep_kernel, decode_kernel,
+ * prefill_kernel, combine_kernel, block_move_kernel) so a profiler's timeline shows them;
+ * off by default.  Without a profiler attached the ranges cost next to nothing.
+ * KVP_E_INVALID_ARG for a null pool. */
+KVP_API kvp_status kv_pool_set_nvtx(kvp_pool* pool, int on);
 
 /* Number of kernels this pool's calls have launched so far (host counter). */
 KVP_API long long kv_pool_launch_count(const kvp_pool* pool);

@@ -154,6 +154,9 @@ def test_workspace_size_and_split_setting(kp):
             with pytest.raises(kp.KVPError):
                 kp.kv_pool_set_decode_ctas(p, bad)
         assert kp.lib.paged_attention_workspace_size(p, 3, 7, 16, 7) == 0     # only 32 query heads
+        kp.kv_pool_set_nvtx(p, True)           # NVTX ranges: a host-side switch, no device work
+        kp.kv_pool_set_nvtx(p, False)
+        assert kp.lib.kv_pool_set_nvtx(None, 1) == -1
     finally:
         kp.kv_pool_destroy(p)
 

@@ -71,3 +71,31 @@ def test_oracle_timing_repeats_until_the_requested_time():
     assert passes >= 1 and wall >= 0.05 and n == 4 * passes
     n1, _, p1 = bench.time_oracle("tiny", 100)   # more rows than the step has: the whole step, once
     assert p1 == 1 and n1 == 7
+
+
+def test_oracle_tasks_cover_the_sample_once():
+    import bench
+    from continuous_batching_paged_step_gb300 import workloads as wl
+    spec = wl.chunked_prefill_step()
+    cu = np.concatenate([[0], np.cumsum(spec.q_lens)])
+    rows = bench.oracle_sample_rows(spec.num_tokens, 3000)
+    tasks = bench.oracle_tasks(cu, spec.ctx_lens, rows, 16)
+    flat = sorted(x for t in tasks for x in t)
+    assert flat == sorted(int(x) for x in rows)
+    for t in tasks:   # each task holds rows of one request
+        reqs = set(int(r) for r in np.searchsorted(cu, t, side="right") - 1)
+        assert len(reqs) == 1
+    cost = [sum(spec.ctx_lens[int(np.searchsorted(cu, x, side="right") - 1)] + x - cu[int(np.searchsorted(cu, x, side="right") - 1)] + 1
+                for x in t) for t in tasks]
+    assert cost == sorted(cost, reverse=True)          # handed out longest first
+
+
+def test_oracle_pool_matches_one_process():
+    import bench
+    rows = bench.oracle_sample_rows(7, 7)
+    t = bench.OracleTimer("tiny", workers=2)
+    try:
+        n, w = t.time_rows(rows)
+    finally:
+        t.close()
+    assert n == 7 and w > 0 and t.workers == 2

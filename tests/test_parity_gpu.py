@@ -10,6 +10,8 @@ import pytest
 import oracle
 from continuous_batching_paged_step_gb300 import workloads as wl
 
+import parity_helpers as ph
+
 pytestmark = pytest.mark.gpu
 
 MAX_ABS, MEAN_ABS = 2e-2, 2e-3
@@ -35,28 +37,6 @@ def _compare(got, want, rows=None, what=""):
     return err.max(), err.mean()
 
 
-def _oracle_pool(inp, fill_bits):
-    spec = inp.spec
-    shape = (spec.num_blocks, spec.n_kv_heads, spec.block_size, spec.head_dim)
-    kc = np.full(shape, fill_bits, np.uint16)
-    vc = np.full(shape, fill_bits, np.uint16)
-    ctx = inp.context_lens
-    cu0 = np.concatenate([[0], np.cumsum(ctx)]).astype(np.int32)
-    kp_ = [k for k in inp.k_prior if k is not None and k.shape[0]]
-    vp_ = [v for v in inp.v_prior if v is not None and v.shape[0]]
-    if kp_:
-        kc, vc = oracle.reference_cache_write(kc, vc, np.concatenate(kp_), np.concatenate(vp_), cu0,
-                                              np.zeros_like(ctx), inp.block_tables, spec.n_kv_heads, spec.head_dim)
-    return oracle.reference_cache_write(kc, vc, inp.k_new, inp.v_new, inp.cu_seqlens_q, inp.context_lens,
-                                        inp.block_tables, spec.n_kv_heads, spec.head_dim)
-
-
-def _pool_bits(step):
-    k = step.pool.k_cache.view(__import__("torch").int16).cpu().numpy().view(np.uint16)
-    v = step.pool.v_cache.view(__import__("torch").int16).cpu().numpy().view(np.uint16)
-    return k, v
-
-
 def _run_full_check(runner, spec, ctas=None):
     inp = wl.make_inputs(spec)
     step = runner.PagedStep(inp, pool_fill_bits=NAN_BITS, decode_ctas=ctas, poison_workspace=True)
@@ -64,8 +44,8 @@ def _run_full_check(runner, spec, ctas=None):
         step.run()
         st, bits = step.error()
         assert (st, bits) == (0, 0)
-        k, v = _pool_bits(step)
-        ok_k, ok_v = _oracle_pool(inp, NAN_BITS)
+        k, v = ph.pool_bits(step)
+        ok_k, ok_v = ph.oracle_pool(inp, NAN_BITS)
         assert np.array_equal(k, ok_k) and np.array_equal(v, ok_v), "pool differs from the oracle's cache write"
         return _compare(step.out_f32(), oracle.step_reference(inp), what=spec.name)
     finally:
@@ -194,7 +174,7 @@ def test_full_size_configs_sampled(runner, name):
         want = oracle.step_reference(inp, rows=rows)
         _compare(step.out_f32(), want, rows=rows, what=name)
         # kv_append bit-exact at the sampled rows: read each row back through the table
-        k, v = _pool_bits(step)
+        k, v = ph.pool_bits(step)
         cu = inp.cu_seqlens_q
         for i in rows[:64]:
             r = int(np.searchsorted(cu, i, side="right") - 1)

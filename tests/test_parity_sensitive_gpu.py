@@ -1,0 +1,77 @@
+"""GPU parity on inputs where every compared block matters.
+
+Two shapings of the long-context step (decode rows over contexts 0 .. 8192, prefill
+chunks after cached prefixes of up to 6144 tokens) run through the C ABI and are
+compared with the fp64 oracle at the benchmark spec's tolerance:
+
+* needles: chosen keys dominate every row that sees them (one in every block of short
+  histories, 16 spread over long ones, at offsets 0 and 15 of their blocks), so a block
+  the kernels skip or read twice moves the output well past the tolerance
+  (test_needle_sensitivity.py shows the oracle itself fails the comparison when one
+  block is dropped or repeated);
+* late peak: scores climb by tens of units along each history, so the decode kernel's
+  lazily moved maximum (moved when a score exceeds it by 2^8) and the prefill kernel's
+  in-TMEM rescale of O fire again and again, up to the last keys.
+
+Each runs with the decode kernel capped at one CTA per SM (0), one CTA (its blocks
+shared out over several waves), 7 CTAs, and 1,024 CTAs (rows split into many pieces).
+Pools start NaN-filled and the workspace poisoned, so a read of an unwritten slot or
+of stale scratch shows up.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from continuous_batching_paged_step_gb300 import workloads as wl
+
+import parity_helpers as ss
+
+pytestmark = pytest.mark.gpu
+
+NAN_BITS = 0x7FC1
+
+
+@pytest.fixture(scope="module")
+def runner():
+    from continuous_batching_paged_step_gb300 import build
+    build.build()
+    from continuous_batching_paged_step_gb300 import runner as r
+    return r
+
+
+@pytest.fixture(scope="module")
+def shaped():
+    base = wl.make_inputs(wl.long_context_step())
+    out = {}
+    ni, _ = wl.plant_needles(base)
+    out["needle"] = ni
+    out["late_peak"] = wl.plant_late_peak(base)
+    res = {}
+    for k, inp in out.items():
+        rows = ss.compare_rows(inp)
+        res[k] = (inp, rows, oracle.step_reference(inp, rows=rows))
+    return res
+
+
+@pytest.mark.parametrize("ctas", [0, 1, 7, 1024])
+@pytest.mark.parametrize("kind", ["needle", "late_peak"])
+def test_sensitive_step(runner, shaped, kind, ctas):
+    inp, rows, want = shaped[kind]
+    step = runner.PagedStep(inp, pool_fill_bits=NAN_BITS, decode_ctas=ctas, poison_workspace=True)
+    try:
+        step.run()
+        assert step.error() == (0, 0)
+        got = step.out_f32()
+        assert np.isfinite(got[rows]).all(), "non-finite output"
+        mx, mn = ss.errors(got[rows], want[rows])
+        err = np.abs(got[rows] - want[rows])
+        worst = np.unravel_index(np.argmax(err), err.shape)
+        assert mx <= ss.MAX_ABS, f"{kind}/{ctas}: max-abs {mx:.3e} at packed row {rows[worst[0]]}, head {worst[1]}"
+        assert mn <= ss.MEAN_ABS, f"{kind}/{ctas}: mean-abs {mn:.3e}"
+        # per request as well: a lost block in one request must not hide in the average
+        for r in range(inp.spec.num_reqs):
+            rr = ss.rows_of_request(inp, r, rows)
+            if rr:
+                assert ss.within_tolerance(got[rr], want[rr]), f"{kind}/{ctas}: request {r}"
+    finally:
+        step.close()
