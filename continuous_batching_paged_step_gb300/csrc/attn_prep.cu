@@ -10,8 +10,12 @@
 //     shares the total out among its CTAs; counters[4] (zeroed here) counts the chunks
 //     of their ranges' tails the decode CTAs have taken.
 //   q_r >= 2 (prefill chunk): one tile per 64 query tokens (two MMA tiles of 32 tokens x
-//     4 query heads of a KV group), emitted last tile first so the longest tiles start
-//     earliest.
+//     4 query heads of a KV group).  The tiles of all chunks are emitted longest first
+//     (by the number of 128-key tiles their last row reads), so that the prefill kernel,
+//     whose CTAs start in list order, ends on its shortest tiles: a chunk after a long
+//     cached prefix would otherwise leave its 50-60-key-tile CTAs for last.  The order
+//     is a counting sort over key-tile counts; tiles with equal counts come in any order
+//     (every tile writes only its own rows).
 // SM split: the decode rows are HBM-bound and the prefill tiles tensor-bound, so the
 // attention kernels run side by side: the decode kernel takes counters[2] CTAs (one per
 // SM) and leaves the other SMs to prefill tiles, which start while the decode runs.  The
@@ -29,6 +33,13 @@ namespace kvp {
 namespace {
 
 constexpr int kPrepThreads = 1024;
+constexpr int kTileBins = 1024;   // key-tile counts of prefill tiles (larger ones share the last bin)
+
+// Key tiles (128 keys) read by the last row of the prefill tile of `ntok` tokens that
+// starts `tok0` tokens into a chunk after `c` cached tokens, as a sort bin.
+__device__ __forceinline__ int tile_bin(int c, int tok0, int ntok) {
+    return min((c + tok0 + ntok - 1) / 128 + 1, kTileBins - 1);
+}
 
 // Cost model of the SM split.  Prefill work is counted in units of one key tile of one
 // prefill CTA (128 keys x 64 query tokens x 4 heads through QK^T, softmax and P.V: about
@@ -81,12 +92,14 @@ __global__ void __launch_bounds__(kPrepThreads) step_prep_kernel(
     __shared__ int2 s_warp[32];
     __shared__ int2 s_base;
     __shared__ float s_w[32];
+    __shared__ int s_hist[kTileBins];    // tiles per bin, then the bin's next output slot
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     grid_dep_launch();
     if (tid == 0) {
         s_ok = (cu[0] == 0 && cu[num_reqs] == num_tokens) ? 1 : 0;
         s_base = make_int2(0, 0);
     }
+    for (int i = tid; i < kTileBins; i += kPrepThreads) s_hist[i] = 0;
     __syncthreads();
     for (int r = tid; r < num_reqs; r += kPrepThreads)
         if (cu[r + 1] < cu[r]) s_ok = 0;
@@ -110,9 +123,11 @@ __global__ void __launch_bounds__(kPrepThreads) step_prep_kernel(
             } else if (q > 1) {
                 n.y = (q + kPrefillTileTokens - 1) / kPrefillTileTokens;
                 for (int t = 0; t < n.y; ++t) {
-                    const int end = c + min(q, (t + 1) * kPrefillTileTokens);   // keys of the tile's last row
+                    const int tok0 = t * kPrefillTileTokens, ntok = min(kPrefillTileTokens, q - tok0);
+                    const int end = c + tok0 + ntok;   // keys of the tile's last row
                     const float u = (float)((end + 127) / 128) + kTileFixedUnits;
                     w_units += u;
+                    atomicAdd(&s_hist[tile_bin(c, tok0, ntok)], 1);
                 }
             }
         }
@@ -129,18 +144,9 @@ __global__ void __launch_bounds__(kPrepThreads) step_prep_kernel(
         const int2 base = s_base;
         const int dx = base.x + wex.x + incl.x - n.x;
         const int dz = base.y + wex.y + incl.y - n.y;
+        (void)dz;
         if (r < num_reqs) {
             page_off[r] = dx;
-        }
-        if (n.y > 0) {
-            if (dz + n.y > max_prefill_tiles) {
-                raise_error(err, kErrBadMeta);
-            } else {
-                for (int t = 0; t < n.y; ++t) {
-                    const int tok0 = (n.y - 1 - t) * kPrefillTileTokens;
-                    pre_tiles[dz + t] = make_int4(r, tok0, min(kPrefillTileTokens, q - tok0), 0);
-                }
-            }
         }
         __syncthreads();
         if (tid == kPrepThreads - 1) s_base = make_int2(dx + n.x, dz + n.y);
@@ -149,14 +155,60 @@ __global__ void __launch_bounds__(kPrepThreads) step_prep_kernel(
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) w_units += __shfl_xor_sync(0xffffffffu, w_units, o);
     if (lane == 0) s_w[warp] = w_units;
+    // Prefill tile order: bins in decreasing key-tile count, each bin's tiles from its first
+    // output slot on (exclusive scan of the counts from the top bin down; kTileBins ==
+    // kPrepThreads, one bin per thread).
+    const int2 tot = s_base;
+    const bool emit = tot.y <= max_prefill_tiles;
+    if (!emit && tid == 0) raise_error(err, kErrBadMeta);
+    {
+        const int bin = kTileBins - 1 - tid;
+        const int cnt = s_hist[bin];
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        __syncthreads();
+        if (lane == 31) s_warp[warp].x = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int wt = s_warp[lane].x;
+            int wi = wt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, wi, o);
+                if (lane >= o) wi += u;
+            }
+            s_warp[lane].x = wi - wt;
+        }
+        __syncthreads();
+        s_hist[bin] = s_warp[warp].x + incl - cnt;
+        __syncthreads();
+    }
+    if (all_ok && emit) {
+        for (int r = tid; r < num_reqs; r += kPrepThreads) {
+            const int q = cu[r + 1] - cu[r];
+            const int c = ctx[r];
+            if (q < 2 || c < 0 || c > max_context_len || q > max_q_len ||
+                (long long)c + q > (long long)max_blocks * kBlockSize)
+                continue;
+            const int nt = (q + kPrefillTileTokens - 1) / kPrefillTileTokens;
+            for (int t = nt - 1; t >= 0; --t) {
+                const int tok0 = t * kPrefillTileTokens, ntok = min(kPrefillTileTokens, q - tok0);
+                const int at = atomicAdd(&s_hist[tile_bin(c, tok0, ntok)], 1);
+                pre_tiles[at] = make_int4(r, tok0, ntok, 0);
+            }
+        }
+    }
     __syncthreads();
     if (tid == 0) {
-        const int2 b = s_base;
         float w = 0.f;
         for (int i = 0; i < kPrepThreads / 32; ++i) w += s_w[i];
-        page_off[num_reqs] = b.x;
-        counters[1] = min(b.y, max_prefill_tiles);
-        counters[2] = decode_sm_share(b.x, w * kNumKvHeads, num_sms);
+        page_off[num_reqs] = tot.x;
+        counters[1] = emit ? tot.y : 0;
+        counters[2] = decode_sm_share(tot.x, w * kNumKvHeads, num_sms);
         counters[3] = 0;
         counters[4] = 0;
     }
