@@ -18,6 +18,7 @@
 namespace kvp {
 cudaError_t configure_decode_kernel();
 cudaError_t configure_prefill_kernel();
+cudaError_t configure_mixed_kernel();
 }  // namespace kvp
 
 struct kvp_pool {
@@ -29,6 +30,7 @@ struct kvp_pool {
     std::vector<int32_t> refcnt;
     int dirty_lo = 1, dirty_hi = 0;  // refcount range changed since the last upload
     int decode_ctas = 0;  // 0: one decode CTA per SM
+    int step_kernel = 0;  // 1: the mixed step kernel instead of the decode + prefill kernels
     // device state (made on first device call)
     int device = -1;
     int num_sms = 0;
@@ -146,7 +148,8 @@ kvp_status ensure_device(kvp_pool* p) {
         ok = cudaHostAlloc(reinterpret_cast<void**>(&p->h_stage[i]), nb * sizeof(int32_t), cudaHostAllocDefault) ==
                  cudaSuccess &&
              cudaEventCreateWithFlags(&p->stage_ev[i], cudaEventDisableTiming) == cudaSuccess;
-    ok = ok && kvp::configure_decode_kernel() == cudaSuccess && kvp::configure_prefill_kernel() == cudaSuccess;
+    ok = ok && kvp::configure_decode_kernel() == cudaSuccess && kvp::configure_prefill_kernel() == cudaSuccess &&
+         kvp::configure_mixed_kernel() == cudaSuccess;
     const int tile_rows = kvp::kBlockSize, block_rows = kvp::kBlockSize * kvp::kNumKvHeads;
     ok = ok && encode_pool_map(&p->tmap_k, p->k_cache, p->num_blocks, tile_rows) &&
          encode_pool_map(&p->tmap_v, p->v_cache, p->num_blocks, tile_rows) &&
@@ -216,6 +219,7 @@ const char* kernel_name(int kind) {
         case KVP_KERNEL_DECODE: return "decode_kernel";
         case KVP_KERNEL_BLOCKS: return "block_move_kernel";
         case KVP_KERNEL_COMBINE: return "combine_kernel";
+        case KVP_KERNEL_MIXED: return "mixed_step_kernel";
     }
     return "kernel";
 }
@@ -476,6 +480,12 @@ kvp_status kv_pool_set_nvtx(kvp_pool* p, int on) {
     return KVP_OK;
 }
 
+kvp_status kv_pool_set_step_kernel(kvp_pool* p, int mixed) {
+    if (!p || (mixed != 0 && mixed != 1)) return KVP_E_INVALID_ARG;
+    p->step_kernel = mixed;
+    return KVP_OK;
+}
+
 kvp_status kv_pool_set_decode_ctas(kvp_pool* p, int ctas) {
     if (!p || ctas < 0 || ctas > kvp::kMaxDecodeCtas) return KVP_E_INVALID_ARG;
     p->decode_ctas = ctas;
@@ -548,16 +558,27 @@ kvp_status paged_attention_step(kvp_pool* p, const void* q, void* out, const int
     a.decode_ctas = p->decode_ctas;
     if (timed_launch(p, KVP_KERNEL_PREP, s, [&] { return kvp::launch_step_prep(a, s); }) != cudaSuccess)
         return KVP_E_CUDA;
-    // decode first; the prefill kernel follows as its programmatic dependent and runs on
-    // the SMs the decode leaves free (the metadata kernel sizes the split)
-    if (timed_launch(p, KVP_KERNEL_DECODE, s, [&] { return kvp::launch_decode(a, &p->tmap_k_blk, &p->tmap_v_blk, s); }) != cudaSuccess)
-        return KVP_E_CUDA;
-    if (max_q_len >= 2 && lay.max_prefill_tiles > 0) {
+    if (p->step_kernel == 1) {
+        // one grid for the decode rows and the prefill tiles (work tickets)
         CUtensorMap tq;
         if (!encode_q_map(&tq, q, num_tokens)) return KVP_E_CUDA;
-        if (timed_launch(p, KVP_KERNEL_PREFILL, s,
-                         [&] { return kvp::launch_prefill(a, &tq, &p->tmap_k, &p->tmap_v, s); }) != cudaSuccess)
+        if (timed_launch(p, KVP_KERNEL_MIXED, s, [&] {
+                return kvp::launch_mixed(a, &tq, &p->tmap_k, &p->tmap_v, &p->tmap_k_blk, &p->tmap_v_blk, s);
+            }) != cudaSuccess)
             return KVP_E_CUDA;
+    } else {
+        // decode first; the prefill kernel follows as its programmatic dependent and runs on
+        // the SMs the decode leaves free (the metadata kernel sizes the split)
+        if (timed_launch(p, KVP_KERNEL_DECODE, s,
+                         [&] { return kvp::launch_decode(a, &p->tmap_k_blk, &p->tmap_v_blk, s); }) != cudaSuccess)
+            return KVP_E_CUDA;
+        if (max_q_len >= 2 && lay.max_prefill_tiles > 0) {
+            CUtensorMap tq;
+            if (!encode_q_map(&tq, q, num_tokens)) return KVP_E_CUDA;
+            if (timed_launch(p, KVP_KERNEL_PREFILL, s,
+                             [&] { return kvp::launch_prefill(a, &tq, &p->tmap_k, &p->tmap_v, s); }) != cudaSuccess)
+                return KVP_E_CUDA;
+        }
     }
     if (timed_launch(p, KVP_KERNEL_COMBINE, s, [&] { return kvp::launch_combine(a, s); }) != cudaSuccess)
         return KVP_E_CUDA;

@@ -99,6 +99,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return mbar_wait_slow(a, parity);
 }
 
+// The whole warp waits; true only if every lane saw the phase complete in time.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
 // True in exactly one lane of the (converged) warp.
 __device__ __forceinline__ bool elect_one() {
     uint32_t p;

@@ -18,7 +18,7 @@ struct StepLayout {
     int max_prefill_tiles;   // (request, 32-token q tile) work items of prefill chunks
     int max_partials;        // split-KV partial slots: request r cut by decode piece p uses r + p
     size_t counters_off;     // int32[8]: 1 = prefill tiles, 2 = decode CTAs, 3 = prefill CTAs done,
-                             // 4 = decode chunks taken
+                             // 4 = decode chunks taken, 5 = mixed step kernel tickets taken
     size_t page_off_off;     // int32 [num_reqs + 1]: first global decode block of each request
     size_t prefill_tiles_off;// int4 {r, first token of tile, tokens in tile, 0}
     size_t part_acc_off;     // float [slot][32 heads][128]  (unnormalised)
@@ -66,6 +66,11 @@ cudaError_t launch_decode(const StepArgs& a, const CUtensorMap* tmap_k, const CU
 cudaError_t launch_combine(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const StepArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
                            const CUtensorMap* tmap_v, cudaStream_t stream);
+// The step's decode rows and prefill tiles in one grid (attn_mixed.cu): the decode
+// kernel's CTAs and the prefill kernel's CTAs, each CTA taking the next work ticket.
+cudaError_t launch_mixed(const StepArgs& a, const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
+                         const CUtensorMap* tmap_v, const CUtensorMap* tmap_k_blk, const CUtensorMap* tmap_v_blk,
+                         cudaStream_t stream);
 
 // Whole-block copies (K and V, 32 KiB each): block i of the launch reads
 // src[kv] + (src_ids_used ? src_ids[i] : i) * 32 KiB and writes dst[kv] + (dst_ids_used ?

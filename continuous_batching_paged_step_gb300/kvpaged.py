@@ -37,6 +37,7 @@ SIGNATURES = {
     "paged_attention_workspace_size": (_SZ, [_P, _I, _I, _I, _I]),
     "paged_attention_step": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _P]),
     "kv_pool_set_decode_ctas": (_I, [_P, _I]),
+    "kv_pool_set_step_kernel": (_I, [_P, _I]),
     "kv_pool_set_nvtx": (_I, [_P, _I]),
     "kv_pool_get_error": (_I, [_P, _P, ctypes.POINTER(ctypes.c_uint32)]),
     "kvp_status_string": (ctypes.c_char_p, [_I]),
@@ -50,7 +51,8 @@ SIGNATURES = {
     "kv_blocks_swap_out": (_I, [_P, _I, _I32P, _P, _P, _P]),
     "kv_blocks_swap_in": (_I, [_P, _I, _P, _P, _I32P, _P]),
 }
-KERNEL_NAMES = ("kv_append", "step_prep", "prefill_tcgen05", "decode_splitkv", "block_move", "splitkv_combine")
+KERNEL_NAMES = ("kv_append", "step_prep", "prefill_tcgen05", "decode_splitkv", "block_move", "splitkv_combine",
+                "mixed_step")
 BLOCK_BYTES = N_KV_HEADS * BLOCK_SIZE * HEAD_DIM * 2   # one block of K (or of V): 32 KiB
 
 
@@ -213,6 +215,12 @@ def kv_pool_set_decode_ctas(pool: int, ctas: int):
 def kv_pool_set_nvtx(pool: int, on: bool):
     """NVTX ranges (domain "kvpaged") around this pool's calls and kernel launches."""
     _check(lib.kv_pool_set_nvtx(pool, 1 if on else 0), "kv_pool_set_nvtx")
+
+
+def kv_pool_set_step_kernel(pool: int, mixed: bool):
+    """Run the step's attention as the mixed step kernel (one grid, work tickets) instead
+    of the decode kernel and the prefill kernel side by side."""
+    _check(lib.kv_pool_set_step_kernel(pool, 1 if mixed else 0), "kv_pool_set_step_kernel")
 
 
 def kv_pool_get_error(pool: int, stream=None):

@@ -27,7 +27,8 @@ def _dev_i32(a: np.ndarray, device) -> torch.Tensor:
 
 class PagedStep:
     def __init__(self, inp: StepInputs, device="cuda", pool_fill_bits: int | None = None,
-                 decode_ctas: int | None = None, fill_prior: bool = True, poison_workspace: bool = False):
+                 decode_ctas: int | None = None, fill_prior: bool = True, poison_workspace: bool = False,
+                 mixed: bool = False):
         spec = inp.spec
         self.inp = inp
         self.device = device
@@ -38,6 +39,8 @@ class PagedStep:
             self.pool.v_cache.view(torch.int16).fill_(fill)
         if decode_ctas is not None:
             kp.kv_pool_set_decode_ctas(self.pool.handle, decode_ctas)
+        if mixed:
+            kp.kv_pool_set_step_kernel(self.pool.handle, True)
         kp.kv_block_claim(self.pool.handle, inp.block_order)
         self.block_tables = _dev_i32(inp.block_tables, device)
         self.cu_seqlens_q = _dev_i32(inp.cu_seqlens_q, device)

@@ -287,9 +287,20 @@ KVP_API size_t paged_attention_noalloc_capacity(void);
 #define KVP_KERNEL_DECODE  3   /* split-KV partials of decode rows cut into several pieces */
 #define KVP_KERNEL_BLOCKS  4   /* block copies of kv_block_cow / kv_blocks_swap_* */
 #define KVP_KERNEL_COMBINE 5   /* merges those partials */
-#define KVP_NUM_KERNELS    6
+#define KVP_KERNEL_MIXED   6   /* the mixed step kernel (decode rows and prefill tiles in one grid) */
+#define KVP_NUM_KERNELS    7
 KVP_API kvp_status kv_pool_enable_timing(kvp_pool* pool, int max_launches);
 KVP_API kvp_status kv_pool_read_timing(kvp_pool* pool, int* counts, float* ms);
+
+/* Which kernels run a step's attention: 0 (the default) launches the decode kernel and the
+ * prefill kernel as its programmatic dependent, side by side on disjoint SMs; 1 launches
+ * the mixed step kernel, one grid whose CTAs take work tickets from a device counter in
+ * the order they start: the decode CTAs' block ranges first, then the prefill (tile, KV
+ * head) items longest first (page "Continuous Batching", section "把 prefill 和 decode 打包在
+ * 一起": one packed pass).  The results are the same up to the order of floating-point
+ * additions (identical per row: both run the same CTA code).  KVP_E_INVALID_ARG for
+ * another value or a null pool.  Host-side setting, no device work. */
+KVP_API kvp_status kv_pool_set_step_kernel(kvp_pool* pool, int mixed);
 
 /* NVTX ranges (domain "kvpaged"): with on != 0, kv_append, paged_attention_step, the
  * block copies and every kernel launch of this pool are wrapped in named ranges

@@ -157,6 +157,12 @@ def test_workspace_size_and_split_setting(kp):
         kp.kv_pool_set_nvtx(p, True)           # NVTX ranges: a host-side switch, no device work
         kp.kv_pool_set_nvtx(p, False)
         assert kp.lib.kv_pool_set_nvtx(None, 1) == -1
+        kp.kv_pool_set_step_kernel(p, True)    # the mixed step kernel: a host-side switch too
+        kp.kv_pool_set_step_kernel(p, False)
+        for bad in (-1, 2):
+            assert kp.lib.kv_pool_set_step_kernel(p, bad) == -1
+        assert kp.lib.kv_pool_set_step_kernel(None, 1) == -1
+        assert kp.paged_attention_workspace_size(p, 300, 8224, 8192) == big
     finally:
         kp.kv_pool_destroy(p)
 

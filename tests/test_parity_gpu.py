@@ -37,9 +37,10 @@ def _compare(got, want, rows=None, what=""):
     return err.max(), err.mean()
 
 
-def _run_full_check(runner, spec, ctas=None):
+def _run_full_check(runner, spec, ctas=None, mixed=False):
+    # mixed: the mixed step kernel (one grid for decode rows and prefill tiles)
     inp = wl.make_inputs(spec)
-    step = runner.PagedStep(inp, pool_fill_bits=NAN_BITS, decode_ctas=ctas, poison_workspace=True)
+    step = runner.PagedStep(inp, pool_fill_bits=NAN_BITS, decode_ctas=ctas, poison_workspace=True, mixed=mixed)
     try:
         step.run()
         st, bits = step.error()
@@ -52,16 +53,18 @@ def _run_full_check(runner, spec, ctas=None):
         step.close()
 
 
-def test_three_request_example(runner):
+@pytest.mark.parametrize("mixed", [False, True], ids=["two_kernels", "mixed_kernel"])
+def test_three_request_example(runner, mixed):
     # page "11.2 连续批处理与 PagedAttention", section 11.2.2: R1 prefill 5 (nothing cached),
     # R2 decode with 7 cached, R3 decode with 3 cached; 64-block pool
-    _run_full_check(runner, wl.tiny_p5_step())
+    _run_full_check(runner, wl.tiny_p5_step(), mixed=mixed)
 
 
-def test_small_mixed_step_all_rows(runner):
+@pytest.mark.parametrize("mixed", [False, True], ids=["two_kernels", "mixed_kernel"])
+def test_small_mixed_step_all_rows(runner, mixed):
     # prefill chunks spanning several 32-token q tiles with ragged tails, one of them after
     # a cached prefix that ends mid-block; decode rows with varied contexts
-    _run_full_check(runner, wl.small_mixed_step())
+    _run_full_check(runner, wl.small_mixed_step(), mixed=mixed)
 
 
 @pytest.mark.parametrize("ctas", [1, 7, 0, 1024])
@@ -72,8 +75,9 @@ def test_decode_split_and_combine(runner, ctas):
     _run_full_check(runner, spec, ctas=ctas)
 
 
+@pytest.mark.parametrize("mixed", [False, True], ids=["two_kernels", "mixed_kernel"])
 @pytest.mark.parametrize("ctas", [1, 2])
-def test_decode_ranges_beyond_staged_ids(runner, ctas):
+def test_decode_ranges_beyond_staged_ids(runner, ctas, mixed):
     # 2,504 decode blocks: with one CTA at a time no range fits the 1,024 blocks a CTA's
     # range may hold, so the blocks are shared out over three waves of one CTA (chunks of
     # a range's tail go to whichever CTA asks first, in any wave); with two CTAs at a time
@@ -81,10 +85,11 @@ def test_decode_ranges_beyond_staged_ids(runner, ctas):
     # chunk rides along, so the metadata kernel's SM split is exercised too.
     spec = wl.StepSpec("long-decode", q_lens=[1, 1, 1, 1, 1, 70], ctx_lens=[8000, 7990, 8016, 7999, 8001, 100],
                        num_blocks=2700, seed=515)
-    _run_full_check(runner, spec, ctas=ctas)
+    _run_full_check(runner, spec, ctas=ctas, mixed=mixed)
 
 
-def test_many_requests(runner):
+@pytest.mark.parametrize("mixed", [False, True], ids=["two_kernels", "mixed_kernel"])
+def test_many_requests(runner, mixed):
     # 5,000 requests, more than every per-step staging capacity: kv_append's and the decode
     # kernel's shared-memory copies of the step metadata (2,048 requests) fall back to global
     # memory, and the combine kernel's CTA pairs each plan more than one round of rows.
@@ -99,17 +104,18 @@ def test_many_requests(runner):
     q_lens[1234], ctx[1234] = 70, 19
     q_lens[4321], ctx[4321] = 40, 0
     spec = wl.StepSpec("many-requests", q_lens=q_lens, ctx_lens=ctx, num_blocks=12288, seed=9091)
-    _run_full_check(runner, spec)
+    _run_full_check(runner, spec, mixed=mixed)
 
 
-def test_edge_cases(runner):
+@pytest.mark.parametrize("mixed", [False, True], ids=["two_kernels", "mixed_kernel"])
+def test_edge_cases(runner, mixed):
     # an empty request in the middle, decode at positions 0 / 15 / 16 / 31 / 32 / 8192,
     # prefill of 2 rows, a 33-row chunk (two q tiles, one row in the second), a chunk whose
     # cached prefix ends exactly on a 128-key tile boundary and one just before it
     q_lens = [1, 1, 0, 1, 1, 1, 1, 2, 33, 40, 17]
     ctx = [0, 15, 9, 16, 31, 32, 8192, 0, 5, 128, 127]
     spec = wl.StepSpec("edges", q_lens=q_lens, ctx_lens=ctx, num_blocks=1200, seed=4242)
-    _run_full_check(runner, spec)
+    _run_full_check(runner, spec, mixed=mixed)
 
 
 def test_chunked_prefill_matches_one_shot(runner):
@@ -159,11 +165,12 @@ def _sample_rows(spec, rng, per_req=3):
     return np.array(sorted(set(int(x) for x in rows)))
 
 
+@pytest.mark.parametrize("mixed", [False, True], ids=["two_kernels", "mixed_kernel"])
 @pytest.mark.parametrize("name", ["mixed", "decode", "chunked"])
-def test_full_size_configs_sampled(runner, name):
+def test_full_size_configs_sampled(runner, name, mixed):
     spec = wl.CONFIGS[name]()
     inp = wl.make_inputs(spec)
-    step = runner.PagedStep(inp)
+    step = runner.PagedStep(inp, mixed=mixed)
     try:
         step.run()
         assert step.error() == (0, 0)
@@ -206,4 +213,4 @@ def test_random_step_shapes(runner, case):
     if spec.num_tokens == 0:
         spec.q_lens[0] = 1
     ctas = [0, 1, 3, 16][case % 4]
-    _run_full_check(runner, spec, ctas=ctas)
+    _run_full_check(runner, spec, ctas=ctas, mixed=case % 3 == 1)

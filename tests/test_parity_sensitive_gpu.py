@@ -14,7 +14,8 @@ compared with the fp64 oracle at the benchmark spec's tolerance:
   in-TMEM rescale of O fire again and again, up to the last keys.
 
 Each runs with the decode kernel capped at one CTA per SM (0), one CTA (its blocks
-shared out over several waves), 7 CTAs, and 1,024 CTAs (rows split into many pieces).
+shared out over several waves), 7 CTAs, and 1,024 CTAs (rows split into many pieces), and
+with the attention run as two kernels side by side or as the mixed step kernel.
 Pools start NaN-filled and the workspace poisoned, so a read of an unwritten slot or
 of stale scratch shows up.
 """
@@ -53,11 +54,12 @@ def shaped():
     return res
 
 
+@pytest.mark.parametrize("mixed", [False, True], ids=["two_kernels", "mixed_kernel"])
 @pytest.mark.parametrize("ctas", [0, 1, 7, 1024])
 @pytest.mark.parametrize("kind", ["needle", "late_peak"])
-def test_sensitive_step(runner, shaped, kind, ctas):
+def test_sensitive_step(runner, shaped, kind, ctas, mixed):
     inp, rows, want = shaped[kind]
-    step = runner.PagedStep(inp, pool_fill_bits=NAN_BITS, decode_ctas=ctas, poison_workspace=True)
+    step = runner.PagedStep(inp, pool_fill_bits=NAN_BITS, decode_ctas=ctas, poison_workspace=True, mixed=mixed)
     try:
         step.run()
         assert step.error() == (0, 0)
