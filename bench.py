@@ -52,8 +52,13 @@ UNIT = "tokens/s"
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 L2_FLUSH_BYTES = 256 << 20
 CSRC = os.path.join(ROOT, "continuous_batching_paged_step_gb300", "csrc")
-KERNEL_SOURCES = {"decode_splitkv": "attn_decode.cu", "prefill_tcgen05": "attn_prefill.cu",
-                  "kv_append": "kv_append.cu", "step_prep": "attn_prep.cu"}
+# the files a kernel's code lives in (its .cu, the device-code header it shares with the
+# mixed step kernel, the common device helpers): a change to any of them makes recorded
+# ncu counters stale
+KERNEL_SOURCES = {"decode_splitkv": ("attn_decode.cu", "attn_decode.cuh", "kvp_device.cuh"),
+                  "splitkv_combine": ("attn_decode.cu", "attn_decode.cuh", "kvp_device.cuh"),
+                  "prefill_tcgen05": ("attn_prefill.cu", "attn_prefill.cuh", "kvp_device.cuh"),
+                  "kv_append": ("kv_append.cu", "kvp_device.cuh"), "step_prep": ("attn_prep.cu", "kvp_device.cuh")}
 
 
 # ------------------------------------------------------------------ workload algebra
@@ -91,8 +96,11 @@ def peaks():
 
 
 def source_sha(kernel):
-    with open(os.path.join(CSRC, KERNEL_SOURCES[kernel]), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel, workload):
