@@ -17,18 +17,23 @@
 // half, 128-byte swizzle), landing in the canonical K-major SW128 layout.
 //
 // Warp roles (12 warps): warp 0 issues the TMA loads of Q (once) and of K tiles into a
-// 3-stage ring, warp 2 those of V tiles into a 2-stage ring; warp 1 owns TMEM (512
-// columns: S/P of tile A at 0, of B at 128, O of A at 256, of B at 384) and issues the
-// MMAs (the warp in step, one elected lane issuing); warps 4-7 run the softmax of tile A
-// and warps 8-11 that of tile B, one thread per MMA row (TMEM lane).  The MMA warp
-// ping-pongs: O_A += P_A V_kt, S_A = Q_A K_{kt+1}^T, O_B += P_B V_kt, S_B = ..., so the
-// softmax of one tile runs while the tensor core works on the other.  Per key tile a
-// softmax thread: reads its whole S row from TMEM in one load,
+// 3-stage ring, warp 2 those of V tiles into a 2-stage ring; warp 1 owns TMEM and issues
+// the MMAs (the warp in step, one elected lane issuing); warps 4-7 run the softmax of
+// tile A and warps 8-11 that of tile B, one thread per MMA row (TMEM lane).  TMEM (512
+// columns): one S buffer shared by the two tiles at 0, P of A at 128 and of B at 192 (bf16
+// pairs, 64 columns each), O of A at 256 and of B at 384.  With P in columns of its own,
+// S is free again as soon as a softmax has loaded it into registers, so the next Q K^T
+// need not wait for the P V of the same tile: per key tile kt the MMA warp issues
+// S = Q_A K_kt^T, then (once the softmax of A has read S) S = Q_B K_kt^T, then the P V of
+// both tiles for key tile kt - 1.  A tile's softmax then runs beside three groups of MMAs
+// (the other tile's Q K^T and both P V) instead of one.  Per key tile a softmax thread:
+// reads its whole S row from TMEM in one load and frees S,
 // keeps a running max m in base 2 (scores x softmax_scale x log2 e) that moves only when
-// the tile's max exceeds it by more than 8 (then O and l are rescaled in place: until
-// then weights stay below 2^8, which bf16 and fp32 hold exactly enough), writes
-// P = 2^(s - m) as bf16 pairs into TMEM over its S columns, and the P V MMA reads P
-// from TMEM as its A operand (V from shared memory, MN-major: keys are the K dimension).
+// the tile's max exceeds it by more than 8 (then O and l are rescaled in place, after the
+// tile's previous P V has completed: until then weights stay below 2^8, which bf16 and
+// fp32 hold exactly enough), writes P = 2^(s - m) as bf16 pairs into its P columns (once
+// the previous P V has read them), and the P V MMA reads P from TMEM as its A operand (V
+// from shared memory, MN-major: keys are the K dimension).
 // End: O / l rounded to bf16 for the tile's valid rows.
 // Masking: key position > row position gets weight 0 (only on key tiles that reach past
 // the tile's first row position); V rows at positions >= ctx + q_len in the last key
@@ -63,7 +68,8 @@ struct __align__(1024) PrefillSmem {
     uint64_t q_full;
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t v_full[kVStages], v_empty[kVStages];
-    uint64_t s_full[2], p_full[2], o_done[2];   // per MMA tile
+    uint64_t s_full[2], p_full[2], pv_done[2];   // per MMA tile
+    uint64_t s_free[2];   // tile t's softmax (4 warps) has read the shared S buffer
     uint64_t mma_done;
     uint32_t tmem_base;
 };
@@ -92,7 +98,8 @@ __device__ __forceinline__ void softmax_tile(PrefillSmem& S, const PrefillArgs& 
     const int tq0 = qpos0 + kMmaTokens * t;          // position of the tile's first token
     const int qpos = row_valid ? tq0 + tl : -1;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t t_s = tmem + t * 128 + lane_off;
+    const uint32_t t_s = tmem + lane_off;
+    const uint32_t t_p = tmem + 128 + t * 64 + lane_off;
     const uint32_t t_o = tmem + 256 + t * 128 + lane_off;
     const float sc = a.scale_log2;
     float m_used = -INFINITY, l = 0.f;
@@ -105,10 +112,15 @@ __device__ __forceinline__ void softmax_tile(PrefillSmem& S, const PrefillArgs& 
         tc_fence_after();
         const int key0 = kt * kKeyTile;
         const bool need_mask = key0 + kKeyTile - 1 > tq0;
-        // the whole S row in one TMEM load
+        // the whole S row in one TMEM load; then S is free for the next Q K^T
         uint32_t sr[128];
         tmem_ld128(t_s, sr);
         tc_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.s_free[t]);
+        // O and the P columns are this tile's previous P V's until it has completed
+        bool pv_clear = kt == 0;
         if (need_mask) {
             const int lim = qpos - key0;   // column i is visible iff i <= lim
 #pragma unroll
@@ -129,6 +141,12 @@ __device__ __forceinline__ void softmax_tile(PrefillSmem& S, const PrefillArgs& 
             const float m_new = fmaxf(m_used, mx_s);
             const float alpha = (m_used == -INFINITY) ? 0.f : fast_exp2(m_used - m_new);
             if (kt > 0) {
+                if (!warp_wait(&S.pv_done[t], (kt - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                pv_clear = true;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t o[32];
@@ -145,7 +163,7 @@ __device__ __forceinline__ void softmax_tile(PrefillSmem& S, const PrefillArgs& 
         }
         const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
         // weights 2^(s * scale - m) as bf16 pairs, packed in place (pair j -> sr[j]), then
-        // written over the S columns in one TMEM store
+        // written into the tile's P columns in one TMEM store
         const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_sub, -m_sub);
         float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
@@ -155,7 +173,14 @@ __device__ __forceinline__ void softmax_tile(PrefillSmem& S, const PrefillArgs& 
             sum2[(i >> 1) & 1] = __fadd2_rn(sum2[(i >> 1) & 1], p);
             sr[i >> 1] = pack_bf16x2(p.x, p.y);
         }
-        tmem_st64(t_s, sr);
+        if (!pv_clear) {
+            if (!warp_wait(&S.pv_done[t], (kt - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+        }
+        tmem_st64(t_p, sr);
         tc_wait_st();
         l += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
         if (zero_v_rows && kt == n_kt - 1 && key0 + kKeyTile > n_keys) {
@@ -179,7 +204,7 @@ __device__ __forceinline__ void softmax_tile(PrefillSmem& S, const PrefillArgs& 
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.p_full[t]);
     }
-    if (ok && warp_wait(&S.o_done[t], 0)) {
+    if (ok && warp_wait(&S.pv_done[t], (nt - 1) & 1)) {
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
         __nv_bfloat16* orow =
@@ -234,18 +259,20 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tmap_q, const CUt
         mbar_init(&S.q_full, 1);
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&S.k_full[s], 1);
-            mbar_init(&S.k_empty[s], 1);
+            mbar_init(&S.k_empty[s], 2);
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&S.v_full[s], 1);
-            mbar_init(&S.v_empty[s], 1);
+            mbar_init(&S.v_empty[s], 2);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&S.s_full[s], 1);
             mbar_init(&S.p_full[s], 4);
-            mbar_init(&S.o_done[s], 1);
+            mbar_init(&S.pv_done[s], 1);
         }
-        mbar_init(&S.mma_done, 1);
+        mbar_init(&S.s_free[0], 4);
+        mbar_init(&S.s_free[1], 4);
+        mbar_init(&S.mma_done, 2);
         fence_barrier_init();
     }
     tc_fence_before();
@@ -321,12 +348,21 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tmap_q, const CUt
                 if (!mbar_wait(full, (kt / nst) & 1)) raise_error(a.err, kErrTimeout);
             }
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        // The whole warp runs the loop in step (waits, descriptor arithmetic: values the
-        // same in every lane), and one elected lane issues each tcgen05 instruction.  With
-        // the loop on lane 0 alone, that thread took ~80 cycles per MMA, more than the
-        // tensor core's 64.
+    } else if (warp == 1 || warp == 3) {
+        // ---------------------------------------------------------------- MMA issuers
+        // Two groups of MMAs per key tile kt:
+        //   X(kt): S = Q_B K_kt^T, then O_A += P_A V_{kt-1}    (issued by warp 1)
+        //   Y(kt): S = Q_A K_{kt+1}^T, then O_B += P_B V_{kt-1} (issued by warp 3)
+        // Each Q K^T waits until the softmax that read the previous S has loaded it, which
+        // it does while the tensor core runs the P V queued behind that Q K^T; a tile's P
+        // for key tile kt - 1 is consumed about a round after its S was produced, so the
+        // softmax runs off the tensor core's critical path.  A warp that has just queued
+        // MMAs sees its next barrier test come back only ~300 cycles later (its shared-
+        // memory operations wait behind its tcgen05 ones); with the groups alternating
+        // between two warps, the other warp's group keeps the tensor core busy meanwhile.
+        // Each warp runs its loop in step (waits, descriptor arithmetic: values the same
+        // in every lane), and one elected lane issues each tcgen05 instruction.
+        const bool xw = warp == 1;
         const bool leader = elect_one();
         constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 128, 1);
@@ -339,71 +375,102 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tmap_q, const CUt
         const uint64_t k_desc0 = smem_desc_sw128(smem_u32(S.k[0][0]), 16, 1024);
         const uint64_t v_desc0 = smem_desc_sw128(smem_u32(S.v[0][0]), kHalfBytes, 1024);
         bool ok = warp_wait(&S.q_full, 0);
-        // Waits and issues are kept apart: each round first waits for everything it
-        // needs (the next K tile, which is normally long there, then this tile's P and
-        // V), then issues P.V and the next Q K^T back to back, so that the tensor core
-        // has 16 MMAs queued while the warp waits for the other tile.
+        // The S buffer's uses in order: Q_A K_0^T, Q_B K_0^T, Q_A K_1^T, ... (only tile A's
+        // when tile B is empty; tile B may have one key tile more than A).  Each Q K^T waits
+        // until the softmax that read the previous use has loaded it: phase j of s_free[t]
+        // is tile t's j-th read.  A warp only ever waits for the phase after one it has
+        // already seen complete, so a parity test cannot be satisfied by an older phase.
+        //   Q_B K_kt^T: s_free[0] phase kt (kt < nA), else s_free[1] phase kt - 1;
+        //   Q_A K_kt^T (kt >= 1): s_free[1] phase kt - 1 (tile B not empty), else s_free[0].
+        auto s_bar_b = [&](int kt) { return kt < nA ? &S.s_free[0] : &S.s_free[1]; };
+        auto s_ph_b = [&](int kt) { return (uint32_t)((kt < nA ? kt : kt - 1) & 1); };
+        auto s_bar_a = [&]() { return nB > 0 ? &S.s_free[1] : &S.s_free[0]; };
         auto wait_k = [&](int kt) -> bool { return warp_wait(&S.k_full[kt % kKStages], (kt / kKStages) & 1); };
-        auto wait_pv = [&](int t, int kt) -> bool {
-            return warp_wait(&S.p_full[t], kt & 1) && warp_wait(&S.v_full[kt % kVStages], (kt / kVStages) & 1);
-        };
+        auto wait_p = [&](int t, int kt) -> bool { return warp_wait(&S.p_full[t], kt & 1); };
+        auto wait_v = [&](int kt) -> bool { return warp_wait(&S.v_full[kt % kVStages], (kt / kVStages) & 1); };
+        auto test_k = [&](int kt) { return mbar_test(&S.k_full[kt % kKStages], (kt / kKStages) & 1); };
+        auto test_p = [&](int t, int kt) { return mbar_test(&S.p_full[t], kt & 1); };
+        auto test_v = [&](int kt) { return mbar_test(&S.v_full[kt % kVStages], (kt / kVStages) & 1); };
+        // K and V stages are released by two commits (k_empty / v_empty count 2): one per
+        // tile that reads the stage, or two by the only one (each commit tracks only the
+        // committing thread's MMAs).
         auto mma_qk = [&](int t, int kt) {
             const int s = kt % kKStages;
             const uint64_t qa = q_desc0 + (uint64_t)t * kStep32K, kb = k_desc0 + (uint64_t)s * kStep32K;
-            const uint32_t d = tmem + t * 128;
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t koff = (uint64_t)((((kk >> 2) * kHalfBytes) + (kk & 3) * 32) >> 4);
-                    tc_mma_f16(d, qa + koff, kb + koff, idesc_qk, kk > 0 ? 1u : 0u);
+                    tc_mma_f16(tmem, qa + koff, kb + koff, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&S.s_full[t]);
-                if (t == 1 || kt >= nB) tc_commit(&S.k_empty[s]);   // last QK that reads this K stage
+                tc_commit(&S.k_empty[s]);
+                if (kt >= (t ? nA : nB)) tc_commit(&S.k_empty[s]);
             }
             __syncwarp();
         };
         auto mma_pv = [&](int t, int kt) {
             const int s = kt % kVStages;
             const uint64_t vb = v_desc0 + (uint64_t)s * kStep32K;
-            const uint32_t d = tmem + 256 + t * 128, pa = tmem + t * 128;
+            const uint32_t d = tmem + 256 + t * 128, pa = tmem + 128 + t * 64;
             const uint32_t acc0 = kt > 0 ? 1u : 0u;
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     tc_mma_f16_ts(d, pa + kk * 8, vb + (uint64_t)((kk * 2048) >> 4), idesc_pv, kk > 0 ? 1u : acc0);
-                if (t == 1 || kt >= nB) tc_commit(&S.v_empty[s]);   // last P V that reads this V stage
+                tc_commit(&S.pv_done[t]);
+                tc_commit(&S.v_empty[s]);
+                if (kt >= (t ? nA : nB)) tc_commit(&S.v_empty[s]);
             }
             __syncwarp();
         };
-        auto commit = [&](uint64_t* bar) {
-            if (leader) tc_commit(bar);
-            __syncwarp();
-        };
-        if (ok && n_kt > 0 && (ok = wait_k(0))) {
-            tc_fence_after();
-            if (nA > 0) mma_qk(0, 0);
-            if (nB > 0) mma_qk(1, 0);
-        }
-        for (int kt = 0; kt < n_kt && ok; ++kt) {
-            const bool more = kt + 1 < n_kt;   // the next K tile is needed by some MMA tile
-            if (kt < nA) {
-                if (!(ok = (!more || wait_k(kt + 1)) && wait_pv(0, kt))) break;
+        // The last key tile's V rows past the keys are zeroed by one tile's softmax before
+        // it announces P; the other tile's P V of that key tile waits for that P too.
+        const int last = n_kt - 1;
+        auto zero_wait = [&](int t, int kt) { return kt == last && t != zero_tile; };
+        // A group's barriers are tested together first (one round trip instead of one per
+        // barrier); only if one of them is not complete yet does the warp wait on them in
+        // turn, the S barrier (normally the last to complete) last, so that the MMAs go
+        // out right after the softmax has read S.
+        if (xw) {
+            for (int kt = 0; kt <= n_kt && ok; ++kt) {
+                const bool qk = kt < nB, pv = kt >= 1 && kt <= nA;
+                if (!qk && !pv) continue;
+                const bool zw = pv && zero_wait(0, kt - 1);
+                const uint32_t ready = (qk ? (kt < nA ? 1u : test_k(kt)) & mbar_test(s_bar_b(kt), s_ph_b(kt)) : 1u) &
+                                       (pv ? test_p(0, kt - 1) & test_v(kt - 1) : 1u) & (zw ? test_p(1, kt - 1) : 1u);
+                if (!__all_sync(0xffffffffu, ready != 0) &&
+                    !(ok = (!pv || (wait_p(0, kt - 1) && wait_v(kt - 1))) && (!zw || wait_p(1, kt - 1)) &&
+                           (!qk || ((kt < nA || wait_k(kt)) && warp_wait(s_bar_b(kt), s_ph_b(kt))))))
+                    break;
                 tc_fence_after();
-                mma_pv(0, kt);
-                if (kt + 1 < nA) mma_qk(0, kt + 1);
-                else commit(&S.o_done[0]);
+                if (qk) mma_qk(1, kt);
+                if (pv) mma_pv(0, kt - 1);
             }
-            if (kt < nB) {
-                if (!(ok = (!more || wait_k(kt + 1)) && wait_pv(1, kt))) break;
+        } else {
+            if (ok && nA > 0 && (ok = wait_k(0))) {
                 tc_fence_after();
-                mma_pv(1, kt);
-                if (kt + 1 < nB) mma_qk(1, kt + 1);
-                else commit(&S.o_done[1]);
+                mma_qk(0, 0);
+            }
+            for (int kt = 0; kt <= n_kt && ok; ++kt) {
+                const bool qk = kt + 1 < nA, pv = kt >= 1 && kt <= nB;
+                if (!qk && !pv) continue;
+                const bool zw = pv && zero_wait(1, kt - 1);
+                const uint32_t ready = (qk ? test_k(kt + 1) & mbar_test(s_bar_a(), kt & 1) : 1u) &
+                                       (pv ? test_p(1, kt - 1) & test_v(kt - 1) : 1u) & (zw ? test_p(0, kt - 1) : 1u);
+                if (!__all_sync(0xffffffffu, ready != 0) &&
+                    !(ok = (!pv || (wait_p(1, kt - 1) && wait_v(kt - 1))) && (!zw || wait_p(0, kt - 1)) &&
+                           (!qk || (wait_k(kt + 1) && warp_wait(s_bar_a(), kt & 1)))))
+                    break;
+                tc_fence_after();
+                if (qk) mma_qk(0, kt + 1);
+                if (pv) mma_pv(1, kt - 1);
             }
         }
         if (!ok && leader) raise_error(a.err, kErrTimeout);
-        // No MMA may still be running when TMEM is released.
-        commit(&S.mma_done);
+        // No MMA may still be running when TMEM is released (mma_done: one commit per warp).
+        if (leader) tc_commit(&S.mma_done);
+        __syncwarp();
         if (!warp_wait(&S.mma_done, 0) && leader) raise_error(a.err, kErrTimeout);
     } else if (warp >= 4) {
         // --------------------------------------------------------- softmax + epilogue

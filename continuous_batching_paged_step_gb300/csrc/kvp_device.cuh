@@ -82,6 +82,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
     return ok != 0;
 }
 
+// Non-blocking: has the phase with the given parity completed?  Several of these can be
+// in flight at once (their latencies overlap), unlike a chain of waits.
+__device__ __forceinline__ uint32_t mbar_test(const uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false (and leaves
 // the barrier alone) if it has not completed within kWaitLimitNs.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity) {
