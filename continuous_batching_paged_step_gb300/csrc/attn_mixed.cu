@@ -15,9 +15,8 @@
 // first.  The ticket counter hands out work in start order whatever order the hardware
 // starts CTAs in.  Split decode rows are merged by the combine kernel after this one.
 //
-// Each ticket is one CTA's life: a persistent form (one CTA per SM looping over prefill
-// items with the rings, barriers and TMEM carried across items) measured slower than a CTA
-// per item, so the prefill items keep the one-CTA-per-item form here too.
+// Each ticket is one CTA's life: a prefill ticket runs the prefill CTA body on exactly the
+// one item it names.
 #include "attn_decode.cuh"
 #include "attn_prefill.cuh"
 
@@ -55,8 +54,7 @@ __global__ void __launch_bounds__(kMixedThreads, 1)
     }
     grid_dep_launch();
     const int item = t - a.decode_slots;
-    prefill_cta(tmap_q, tmap_k, tmap_v, a.p, *reinterpret_cast<PrefillSmem*>(base), item / kNumKvHeads,
-                item % kNumKvHeads);
+    prefill_cta(tmap_q, tmap_k, tmap_v, a.p, *reinterpret_cast<PrefillSmem*>(base), item, nullptr);
 }
 
 }  // namespace

@@ -7,8 +7,10 @@ namespace {
 
 // Launched right after the decode kernel, as its programmatic dependent: CTAs start as
 // soon as every decode CTA has passed its own wait for the step's metadata kernel (so the
-// work list and the appended K/V are complete) and take the SMs the decode leaves free.
-// The grid finishes only after the decode grid has: its last CTA to leave waits for it.
+// work list and the appended K/V are complete) and take the SMs the decode leaves free,
+// at most one per SM; each takes work items from the step's counter until none are left,
+// so CTAs that start late (on SMs the decode frees) still find work.  The grid finishes
+// only after the decode grid has: its last CTA to leave waits for it.
 __global__ void __launch_bounds__(kPreThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a) {
@@ -16,12 +18,10 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     PrefillSmem& S =
         *reinterpret_cast<PrefillSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     grid_dep_launch();
-    // blockIdx.x = KV head, blockIdx.y = tile: CTAs start in work-list order (longest first)
-    prefill_cta(tmap_q, tmap_k, tmap_v, a, S, blockIdx.y, blockIdx.x);
+    prefill_cta(tmap_q, tmap_k, tmap_v, a, S, -1, a.next_item);
     __syncthreads();
     if (threadIdx.x == 0) {
-        const int total = gridDim.x * gridDim.y;
-        if (atomicAdd(a.done, 1) == total - 1) grid_dep_wait();
+        if (atomicAdd(a.done, 1) == (int)gridDim.x - 1) grid_dep_wait();
     }
 }
 
@@ -32,9 +32,10 @@ cudaError_t launch_prefill(const StepArgs& a, const CUtensorMap* tmap_q, const C
     const StepLayout& L = a.lay;
     if (L.max_prefill_tiles <= 0 || a.max_q_len < 2) return cudaSuccess;
     const PrefillArgs pa = make_prefill_args(a);
-    dim3 grid(kNumKvHeads, L.max_prefill_tiles);
+    const long long items = (long long)L.max_prefill_tiles * kNumKvHeads;
+    const int grid = (int)(items < a.num_sms ? items : a.num_sms);
     const size_t smem = sizeof(PrefillSmem) + 1024;
-    return launch_pdl(prefill_kernel, grid, dim3(kPreThreads), smem, stream, *tmap_q, *tmap_k, *tmap_v, pa);
+    return launch_pdl(prefill_kernel, dim3(grid), dim3(kPreThreads), smem, stream, *tmap_q, *tmap_k, *tmap_v, pa);
 }
 
 cudaError_t configure_prefill_kernel() {

@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(kPrepThreads) step_prep_kernel(
         counters[3] = 0;
         counters[4] = 0;
         counters[5] = 0;
+        counters[6] = 0;
     }
     // This kernel reads nothing the previous one (kv_append) writes, so it ran alongside
     // it; it finishes only after that kernel has, so that later kernels, which wait for

@@ -18,7 +18,8 @@ struct StepLayout {
     int max_prefill_tiles;   // (request, 32-token q tile) work items of prefill chunks
     int max_partials;        // split-KV partial slots: request r cut by decode piece p uses r + p
     size_t counters_off;     // int32[8]: 1 = prefill tiles, 2 = decode CTAs, 3 = prefill CTAs done,
-                             // 4 = decode chunks taken, 5 = mixed step kernel tickets taken
+                             // 4 = decode chunks taken, 5 = mixed step kernel tickets taken,
+                             // 6 = prefill work items claimed
     size_t page_off_off;     // int32 [num_reqs + 1]: first global decode block of each request
     size_t prefill_tiles_off;// int4 {r, first token of tile, tokens in tile, 0}
     size_t part_acc_off;     // float [slot][32 heads][128]  (unnormalised)
