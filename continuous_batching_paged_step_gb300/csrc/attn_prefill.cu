@@ -17,8 +17,15 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     PrefillSmem& S =
         *reinterpret_cast<PrefillSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ int s_first;
     grid_dep_launch();
-    prefill_cta(tmap_q, tmap_k, tmap_v, a, S, -1, a.next_item);
+    // the CTA's first item, claimed before any set-up: a CTA that finds none leaves at once
+    if (threadIdx.x == 0) {
+        const int k = atomicAdd(a.next_item, 1);
+        s_first = k < __ldcg(&a.counters[1]) * kNumKvHeads ? k : -1;
+    }
+    __syncthreads();
+    if (s_first >= 0) prefill_cta(tmap_q, tmap_k, tmap_v, a, S, s_first, a.next_item);
     __syncthreads();
     if (threadIdx.x == 0) {
         if (atomicAdd(a.done, 1) == (int)gridDim.x - 1) grid_dep_wait();
