@@ -118,6 +118,51 @@ def test_edge_cases(runner, mixed):
     _run_full_check(runner, spec, mixed=mixed)
 
 
+def _many_items_spec(seed=0xC0FFEE + 31):
+    # 60 short prefill chunks after cached prefixes chosen around 128-key tile edges, plus a
+    # few decode rows: several hundred (64-token tile, KV head) work items, so the prefill
+    # kernel's CTAs take several items each, one after another
+    rng = np.random.default_rng(seed)
+    q_lens, ctx = [], []
+    for _ in range(60):
+        k = int(rng.integers(1, 5))
+        ctx.append(int(rng.choice([0, 37, 88, 128 * k - 40, 128 * k - 33, 128 * k - 1, 128 * k + 3])))
+        q_lens.append(int(rng.integers(2, 200)))
+    q_lens += [1] * 6
+    ctx += [int(c) for c in rng.integers(10, 900, size=6)]
+    num_blocks = sum(-(-(c + q) // 16) for c, q in zip(ctx, q_lens)) + 64
+    return wl.StepSpec("many-prefill-items", q_lens=q_lens, ctx_lens=ctx, num_blocks=num_blocks, seed=seed)
+
+
+def _tile_shapes(spec):
+    # per (request, 64-token tile): the key tiles (of 128) that its two 32-token halves read
+    shapes = []
+    for q, c in zip(spec.q_lens, spec.ctx_lens):
+        if q < 2:
+            continue
+        for tok0 in range(0, q, 64):
+            nt = min(64, q - tok0)
+            na, nb = min(32, nt), nt - min(32, nt)
+            pa = (c + tok0 + na - 1) // 128 + 1
+            pb = (c + tok0 + 32 + nb - 1) // 128 + 1 if nb else 0
+            shapes.append((pa, pb))
+    return shapes
+
+
+@pytest.mark.parametrize("mixed", [False, True], ids=["two_kernels", "mixed_kernel"])
+def test_prefill_items_in_sequence(runner, mixed):
+    # The prefill kernel's CTAs carry their rings, barrier phases and TMEM from one work item
+    # to the next: items whose second half is empty, reads the same key tiles as the first,
+    # or reads one key tile more, in every order, several per CTA.
+    spec = _many_items_spec()
+    shapes = _tile_shapes(spec)
+    assert len(shapes) * 8 > 2 * 152
+    assert sum(pb == 0 for _, pb in shapes) >= 5
+    assert sum(pb == pa for pa, pb in shapes) >= 5
+    assert sum(pb == pa + 1 for pa, pb in shapes) >= 5
+    _run_full_check(runner, spec, mixed=mixed)
+
+
 def test_chunked_prefill_matches_one_shot(runner):
     # The same 300-token prompt run as chunks of 100, 150 and 50 over three steps through
     # the pool equals one-shot causal prefill (chunked prefill, page "Continuous Batching
