@@ -152,6 +152,10 @@ __global__ void __launch_bounds__(kNumQHeads / kParts * 32) combine_kernel(const
         }
         __syncthreads();   // S.job and S.n_job are rewritten next round
     }
+    // What follows in the stream (the next step's kernels: its metadata kernel resets the work
+    // counters and rewrites the work lists) starts only once the step's attention kernels have
+    // completed; a CTA with no rows to merge has not waited for them above.
+    grid_dep_wait();
     grid_dep_launch();
 }
 

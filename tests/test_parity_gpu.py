@@ -163,6 +163,38 @@ def test_prefill_items_in_sequence(runner, mixed):
     _run_full_check(runner, spec, mixed=mixed)
 
 
+@pytest.mark.parametrize("mixed", [False, True], ids=["two_kernels", "mixed_kernel"])
+def test_back_to_back_attention_calls_share_workspace(runner, mixed):
+    # Three attention calls in a row on one workspace, nothing between them (each into its
+    # own output): a call's metadata kernel resets the work counters and rewrites the tile
+    # list, so it must not start while the previous call's kernels still read them.  The
+    # step has prefill chunks and no decode rows, so the combine kernel has nothing to merge.
+    import torch
+    spec = wl.StepSpec("prefill-only", q_lens=[1536, 1000, 500], ctx_lens=[1536, 0, 333], num_blocks=512,
+                       seed=0xC0FFEE + 33)
+    inp = wl.make_inputs(spec)
+    step = runner.PagedStep(inp, pool_fill_bits=NAN_BITS, poison_workspace=True, mixed=mixed)
+    try:
+        step.append()
+        nan = int(np.array([NAN_BITS], dtype=np.uint16).view(np.int16)[0])
+        outs = [torch.empty_like(step.out) for _ in range(3)]
+        for o in outs:
+            o.view(torch.int16).fill_(nan)
+        torch.cuda.synchronize()
+        from continuous_batching_paged_step_gb300 import kvpaged as kp
+        for o in outs:
+            kp.paged_attention_step(step.pool.handle, step.q, o, step.cu_seqlens_q, step.context_lens,
+                                    step.block_tables, step.max_q_len, step.max_context_len, step.softmax_scale,
+                                    step.workspace)
+        assert step.error() == (0, 0)
+        want = oracle.step_reference(inp)
+        for i, o in enumerate(outs):
+            got = o.float().cpu().numpy().reshape(spec.num_tokens, spec.n_q_heads, spec.head_dim)
+            _compare(got, want, what=f"call {i}")
+    finally:
+        step.close()
+
+
 def test_chunked_prefill_matches_one_shot(runner):
     # The same 300-token prompt run as chunks of 100, 150 and 50 over three steps through
     # the pool equals one-shot causal prefill (chunked prefill, page "Continuous Batching
