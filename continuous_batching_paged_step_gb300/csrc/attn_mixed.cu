@@ -1,22 +1,20 @@
-// Mixed step kernel: one launch for a step's decode rows and prefill tiles.
+// Mixed step kernel: one persistent launch for a step's decode rows and prefill tiles.
 //
 // Page "Continuous Batching" (k4i.top), section "把 prefill 和 decode 打包在一起", and
 // page "11.2 连续批处理与 PagedAttention", section 11.2.2 (Figure 11-3): a step's prefill
-// chunks and decode rows are one packed pass.  This kernel gives that pass one grid: each
-// CTA, once the step's metadata kernel is complete, takes the next work ticket from a
-// device counter, and the ticket names its work:
+// chunks and decode rows are one packed pass.  This kernel gives that pass one grid of
+// the decode launch's size (whole waves of one CTA per SM).  Each CTA, once the step's
+// metadata kernel is complete, takes a work ticket from a device counter:
 //   tickets [0, D): decode CTA t of D (the decode kernel's CTA body: its block range with
-//     the 20 % tail handed out as chunks through a second counter; CTAs beyond the share
-//     of SMs the metadata kernel gives the decode leave at once);
-//   tickets [D, D + 8 n): prefill item t - D = (tile (t - D) / 8, KV head (t - D) % 8) of
-//     the metadata kernel's longest-first tile list (the prefill kernel's CTA body).
-// CTAs take tickets in the order they start, so the decode ranges start first, spread over
-// the GPU, and prefill items fill the SMs the decode leaves and those it frees, longest
-// first.  The ticket counter hands out work in start order whatever order the hardware
-// starts CTAs in.  Split decode rows are merged by the combine kernel after this one.
-//
-// Each ticket is one CTA's life: a prefill ticket runs the prefill CTA body on exactly the
-// one item it names.
+//     the 20 % tail handed out as chunks through a second counter; tickets beyond the
+//     share of SMs the metadata kernel gives the decode have no range);
+// and then, whatever its ticket, takes prefill work items (tile, KV head) from a third
+// counter, in the metadata kernel's longest-first order, until none are left (the prefill
+// kernel's CTA body, its rings, barriers and TMEM carried from item to item).  CTAs take
+// tickets in the order they start, so the decode ranges start first, spread over the GPU;
+// the CTAs without a range start on prefill items at once, and every decode CTA joins them
+// when its range is done, so the prefill tail runs on every SM.  Split decode rows are
+// merged by the combine kernel after this one.
 #include "attn_decode.cuh"
 #include "attn_prefill.cuh"
 
@@ -50,11 +48,18 @@ __global__ void __launch_bounds__(kMixedThreads, 1)
     const int t = s_ticket;
     if (t < a.decode_slots) {
         decode_cta(tmap_k_blk, tmap_v_blk, a.d, *reinterpret_cast<DecodeSmem*>(base), t, a.decode_slots);
-        return;
+        __syncthreads();   // every warp is done with the decode body's shared memory
     }
     grid_dep_launch();
-    const int item = t - a.decode_slots;
-    prefill_cta(tmap_q, tmap_k, tmap_v, a.p, *reinterpret_cast<PrefillSmem*>(base), item, nullptr);
+    // prefill items until none are left, the first claimed before any set-up
+    __shared__ int s_first;
+    if (threadIdx.x == 0) {
+        const int k = atomicAdd(a.p.next_item, 1);
+        s_first = k < __ldcg(&a.p.counters[1]) * kNumKvHeads ? k : -1;
+    }
+    __syncthreads();
+    if (s_first >= 0)
+        prefill_cta(tmap_q, tmap_k, tmap_v, a.p, *reinterpret_cast<PrefillSmem*>(base), s_first, a.p.next_item);
 }
 
 }  // namespace
@@ -69,7 +74,13 @@ cudaError_t launch_mixed(const StepArgs& a, const CUtensorMap* tmap_q, const CUt
     m.p = make_prefill_args(a);
     int32_t* counters = reinterpret_cast<int32_t*>(a.ws + a.lay.counters_off);
     m.ticket = counters + 5;
-    const long long grid = (long long)m.decode_slots + (prefill ? (long long)a.lay.max_prefill_tiles * kNumKvHeads : 0);
+    // the decode launch's size; at least as many CTAs as prefill items run at once
+    long long grid = m.decode_slots;
+    if (prefill) {
+        const long long items = (long long)a.lay.max_prefill_tiles * kNumKvHeads;
+        const long long want = items < a.num_sms ? items : a.num_sms;
+        if (grid < want) grid = want;
+    }
     return launch_pdl(mixed_step_kernel, dim3((unsigned)grid), dim3(kMixedThreads), kMixedSmemBytes, stream, *tmap_q,
                       *tmap_k, *tmap_v, *tmap_k_blk, *tmap_v_blk, m);
 }
