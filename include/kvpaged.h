@@ -294,10 +294,11 @@ KVP_API kvp_status kv_pool_read_timing(kvp_pool* pool, int* counts, float* ms);
 
 /* Which kernels run a step's attention: 0 (the default) launches the decode kernel and the
  * prefill kernel as its programmatic dependent, side by side on disjoint SMs; 1 launches
- * the mixed step kernel, one grid whose CTAs take work tickets from a device counter in
- * the order they start: the decode CTAs' block ranges first, then the prefill (tile, KV
- * head) items longest first (page "Continuous Batching", section "把 prefill 和 decode 打包在
- * 一起": one packed pass).  The results are the same up to the order of floating-point
+ * the mixed step kernel, one persistent grid whose CTAs take a work ticket from a device
+ * counter in the order they start (the decode CTAs' block ranges go to the first tickets)
+ * and then take prefill (tile, KV head) items, longest first, from another counter until
+ * none are left (page "Continuous Batching", section "把 prefill 和 decode 打包在一起": one
+ * packed pass).  The results are the same up to the order of floating-point
  * additions (identical per row: both run the same CTA code).  KVP_E_INVALID_ARG for
  * another value or a null pool.  Host-side setting, no device work. */
 KVP_API kvp_status kv_pool_set_step_kernel(kvp_pool* pool, int mixed);
