@@ -16,9 +16,9 @@
 // each block's (block, head g) 4 KiB tile is fetched by two 2-D TMA loads (one per 64-dim
 // half, 128-byte swizzle), landing in the canonical K-major SW128 layout.
 //
-// A CTA takes items one after another (the prefill kernel: from a device counter, in the
-// metadata kernel's longest-first order, until none are left; the mixed step kernel: the
-// one item its ticket names).  The rings, barriers and TMEM carry over from item to item
+// A CTA takes items one after another from a device counter, in the metadata kernel's
+// longest-first order, until none are left (in the mixed step kernel, after the decode
+// range its ticket may give it).  The rings, barriers and TMEM carry over from item to item
 // and every role runs ahead into the next item as soon as its part of the current one is
 // done, so a CTA pays its start-up (TMEM, barriers, the first loads) once.
 //
