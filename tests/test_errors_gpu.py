@@ -44,27 +44,32 @@ def test_write_into_shared_block_is_refused(mods):
         step.close()
 
 
-def test_bad_block_id_is_flagged_and_others_survive(mods):
+@pytest.mark.parametrize("mixed", [False, True], ids=["two_kernels", "mixed_kernel"])
+@pytest.mark.parametrize("bad", [1, 2], ids=["decode_row", "prefill_chunk"])
+def test_bad_block_id_is_flagged_and_others_survive(mods, bad, mixed):
     kp, runner = mods
     import torch
     inp = wl.make_inputs(_small())
-    step = runner.PagedStep(inp)
+    step = runner.PagedStep(inp, mixed=mixed)
     try:
         step.run()
         good = step.out_f32()
         assert step.error() == (0, 0)
-        # corrupt one entry of request 1's table (a page it reads, not one it writes)
-        step.block_tables[1, 0] = 10 ** 6
+        # corrupt one entry of request `bad`'s table (a cached page it reads, not one it
+        # writes): request 1 is a decode row, request 2 a prefill chunk
+        step.block_tables[bad, 0] = 10 ** 6
         step.out.zero_()
         step.attend()
         st, bits = step.error()
         assert bits & kp.ERRBIT_BAD_BLOCK
         got = step.out_f32()
         cu = inp.cu_seqlens_q
-        for r in (0, 2):
+        for r in (0, 1, 2):
+            if r == bad:
+                continue
             s, e = cu[r], cu[r + 1]
             assert np.array_equal(got[s:e], good[s:e])
-        step.block_tables[1, 0] = int(inp.block_tables[1, 0])
+        step.block_tables[bad, 0] = int(inp.block_tables[bad, 0])
     finally:
         step.close()
 
