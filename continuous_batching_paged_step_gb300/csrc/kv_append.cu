@@ -33,6 +33,10 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4* __restrict_
     __shared__ int32_t s_cu[kAppendSmemReqs + 1];
     __shared__ int32_t s_ctx[kAppendSmemReqs];
     grid_dep_launch();   // the step's metadata kernel does not read the pool
+    // Launched as a programmatic dependent of whatever precedes it in the stream (normally the
+    // previous step's last kernel), so its CTAs are resident when that kernel ends; nothing is
+    // read or written before that kernel has completed.
+    grid_dep_wait();
     const int lane = threadIdx.x & 31;
     const int i = blockIdx.x * kAppendRowsPerCta + (threadIdx.x >> 5);
     // The row's K and V first: their loads do not depend on where the row goes, so they
@@ -109,10 +113,9 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t
                              cudaStream_t stream) {
     if (num_tokens <= 0) return cudaSuccess;
     const int grid = (num_tokens + kAppendRowsPerCta - 1) / kAppendRowsPerCta;
-    kv_append_kernel<<<grid, 256, 0, stream>>>(
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), cu, ctx, tables, max_blocks, num_reqs,
-        num_tokens, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), refcnt, num_blocks, err);
-    return cudaGetLastError();
+    return launch_pdl(kv_append_kernel, dim3(grid), dim3(256), 0, stream, static_cast<const uint4*>(k_new),
+                      static_cast<const uint4*>(v_new), cu, ctx, tables, max_blocks, num_reqs, num_tokens,
+                      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), refcnt, num_blocks, err);
 }
 
 }  // namespace kvp
